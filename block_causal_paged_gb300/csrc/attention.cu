@@ -1,0 +1,1203 @@
+// Block-causal attention over a paged KV cache, sm_103a (tcgen05 + TMA).
+//
+// One persistent CTA per SM walks a static list of work items.  An item is a
+// block of up to 256 query rows (two M-tiles of 128 rows) that share one KV
+// head, plus the sequence of 64-key tiles those rows attend.  Rows are
+// (token, head) pairs: for decode and multicanvas the G query heads of one KV
+// head are packed into the rows (rows = tokens x G, so K/V is read once per
+// group); for prefill each M-tile is one head over 128 tokens.
+//
+// The visibility rule ("Inference for Interpretable Text-Diffusion Models",
+// "Background"; "Inference: Fewer, smaller forwards", "Advancement 13") is
+// evaluated per row as a key-position limit: a query at position q sees key
+// position k iff k < lim(q), lim(q) = P0 if q < P0 else P0 + D*(floor((q-P0)/D)+1).
+// Each KV tile is classified against the item's rows ("FlexAttention with
+// Aligned Tiles"): fully included (no mask arithmetic), partially included
+// (elementwise k < lim(q)) or fully excluded (not emitted: no load, no math).
+//
+// Warp roles (384 threads):
+//   warp 3      planner  : enumerates items/tiles, reads page tables and
+//                          positions, classifies tiles, writes records into a
+//                          small shared-memory ring
+//   warp 0      loader   : TMA loads of Q and of K/V page boxes into a ring of
+//                          shared-memory stages (ragged 16-key chunks are
+//                          copied by the warp's lanes with zero fill)
+//   warp 1      MMA      : one thread issues tcgen05.mma: S = Q K^T into TMEM,
+//                          O += P V into TMEM (the two M-tiles ping-pong)
+//   warp 2      TMEM allocation / release
+//   warps 4-7   softmax for M-tile 0, warps 8-11 for M-tile 1: read S rows
+//               from TMEM, mask, online softmax (lazy rescale of O), write P
+//               (bf16) to shared memory, final normalisation and store.
+// Every wait is bounded; on timeout the CTA records BCA_ERR_DEVICE_TIMEOUT,
+// drains its copies and MMAs, frees TMEM and exits.
+#include <climits>
+#include <cstdint>
+
+#include "bca_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace bca {
+namespace {
+
+constexpr int kNumRec = 8;
+constexpr int kRecConsumers = 10;  // loader + MMA + 8 softmax warps
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+constexpr int kErrTimeout = -18;
+constexpr int kErrPageOob = -16;
+constexpr int kErrBadLength = -17;
+
+enum RecKind : int { kRecItem = 0, kRecTile = 1, kRecEnd = 2 };
+
+// Record ring entry (128 bytes).  Item fields:
+enum : int {
+  I_KIND = 0, I_NT = 1, I_NM = 2, I_QMODE = 3, I_QTOK = 4 /*2*/, I_QHEAD = 6 /*2*/,
+  I_NTOK = 8 /*2*/, I_QBASE = 10 /*2*/, I_P0 = 12, I_DBLK = 13, I_SPLIT = 14
+};
+// Tile fields:
+enum : int {
+  T_KIND = 0, T_SRC = 1, T_FULL = 2, T_NVALID = 3, T_HEAD = 4, T_KMODE = 5, T_KBASE = 6,
+  T_COORD = 8 /*4*/, T_KOFF = 12 /*4*/
+};
+struct __align__(16) Rec {
+  int32_t w[32];
+};
+
+template <int HD>
+struct Cfg {
+  static constexpr int kHalves = HD / 64;                 // 128-byte column blocks of a row
+  static constexpr int kQBytes = kHalves * 16384;         // 128 rows of Q
+  static constexpr int kPBytes = 16384;                   // 128 rows x 64 keys of P (bf16)
+  static constexpr int kSlotBytes = kHalves * 8192;       // 64 keys of K or V
+  static constexpr int kStages = HD == 128 ? 7 : 14;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;
+  static constexpr int kOffKV = kOffP + 2 * kPBytes;
+  static constexpr int kOffRec = kOffKV + kStages * kSlotBytes;
+  static constexpr int kNumBars = 2 * kNumRec + 2 * kStages + 12 + 1;
+  static constexpr int kOffBar = kOffRec + kNumRec * (int)sizeof(Rec);
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 64;
+  static constexpr int kSmemAlloc = kBytes + 1024;  // base is aligned up to 1024 in the kernel
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kColS = 0;     // S of M-tile m at column 64*m
+  static constexpr int kColO = 128;   // O of M-tile m at column 128 + HD*m
+  static_assert(kColO + 2 * HD <= (int)kTmemCols, "TMEM plan");
+  static_assert(kSmemAlloc <= 232448, "shared memory plan");
+};
+
+struct Bars {
+  uint64_t* rec_full;
+  uint64_t* rec_empty;
+  uint64_t* kv_full;
+  uint64_t* kv_empty;
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* s_full;
+  uint64_t* p_full;
+  uint64_t* o_full;
+  uint64_t* o_empty;
+  uint64_t* drain;
+};
+
+struct Ctx {
+  uint8_t* smem;
+  Rec* ring;
+  Bars bar;
+  volatile int* abort_flag;
+  uint32_t tmem;
+};
+
+__device__ __forceinline__ void record_error(const AttnParams& p, int code) {
+  atomicCAS(&p.hdr->status, 0, code);
+}
+
+__device__ __forceinline__ void give_up(const Ctx& c, const AttnParams& p) {
+  *c.abort_flag = 1;
+  record_error(p, kErrTimeout);
+}
+
+__device__ __forceinline__ bool wait_bar(const Ctx& c, const AttnParams& p, uint64_t* bar,
+                                         uint32_t parity) {
+  if (mbar_wait(bar, parity, c.abort_flag, kWaitTimeoutNs)) return true;
+  give_up(c, p);
+  return false;
+}
+
+// Whole-warp wait with a warp-uniform outcome.
+__device__ __forceinline__ bool wait_bar_warp(const Ctx& c, const AttnParams& p, uint64_t* bar,
+                                              uint32_t parity) {
+  const bool ok = wait_bar(c, p, bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Key-position limit of a query at position q (block rule).
+__device__ __forceinline__ int row_limit(int q, int P0, int D) {
+  if (q < P0) return P0;
+  return P0 + D * ((q - P0) / D + 1);
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_min(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_max(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ long long warp_excl_scan_ll(long long v, int lane) {
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x - v;
+}
+
+// ============================================================================
+// planner (warp 3)
+// ============================================================================
+struct Planner {
+  const AttnParams& p;
+  const Ctx& c;
+  int lane;
+  uint32_t idx = 0;   // records written
+  bool ok = true;
+  unsigned long long n_full = 0, n_partial = 0, n_skip = 0;
+  int page_err = 0;
+
+  __device__ Planner(const AttnParams& p_, const Ctx& c_, int lane_) : p(p_), c(c_), lane(lane_) {}
+
+  // Wait for a free ring entry; returns it (all lanes get the pointer).
+  __device__ Rec* acquire() {
+    const uint32_t slot = idx % kNumRec;
+    if (!wait_bar_warp(c, p, &c.bar.rec_empty[slot], ((idx / kNumRec) & 1) ^ 1)) {
+      ok = false;
+      return nullptr;
+    }
+    return &c.ring[slot];
+  }
+  __device__ void publish() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.bar.rec_full[idx % kNumRec]);
+    __syncwarp();
+    ++idx;
+  }
+  __device__ void emit_end() {
+    Rec* r = acquire();
+    if (!r) return;
+    if (lane == 0) r->w[I_KIND] = kRecEnd;
+    publish();
+  }
+
+  // Emit one tile record.  coord[i]: per 16-key chunk, pool row / dense token
+  // coordinate (already out of range for chunks with no valid key).
+  __device__ void emit_tile(int src, int full, int nvalid, int head, int kmode, int kbase,
+                            const int (&coord)[4], const int (&koff)[4]) {
+    Rec* r = acquire();
+    if (!r) return;
+    if (lane == 0) {
+      r->w[T_KIND] = kRecTile;
+      r->w[T_SRC] = src;
+      r->w[T_FULL] = full;
+      r->w[T_NVALID] = nvalid;
+      r->w[T_HEAD] = head;
+      r->w[T_KMODE] = kmode;
+      r->w[T_KBASE] = kbase;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        r->w[T_COORD + i] = coord[i];
+        r->w[T_KOFF + i] = koff[i];
+      }
+    }
+    publish();
+    if (full) ++n_full; else ++n_partial;
+  }
+
+  __device__ void emit_item(int n_tiles, int n_m, int qmode, const int (&qtok)[2],
+                            const int (&qhead)[2], const int (&ntok)[2], const int (&qbase)[2],
+                            int P0, int Dblk, int split) {
+    Rec* r = acquire();
+    if (!r) return;
+    if (lane == 0) {
+      r->w[I_KIND] = kRecItem;
+      r->w[I_NT] = n_tiles;
+      r->w[I_NM] = n_m;
+      r->w[I_QMODE] = qmode;
+      for (int m = 0; m < 2; ++m) {
+        r->w[I_QTOK + m] = qtok[m];
+        r->w[I_QHEAD + m] = qhead[m];
+        r->w[I_NTOK + m] = ntok[m];
+        r->w[I_QBASE + m] = qbase[m];
+      }
+      r->w[I_P0] = P0;
+      r->w[I_DBLK] = Dblk;
+      r->w[I_SPLIT] = split;
+    }
+    publish();
+  }
+
+  // Page id of logical key position k of sequence b (all lanes call with
+  // their own k); returns -1 for an out-of-range id and flags the error.
+  __device__ int page_of(int b, int k) {
+    const int pidx = k / p.S;
+    int page = -1;
+    if (pidx >= 0 && pidx < p.max_pages) page = __ldg(p.page_table + (size_t)b * p.max_pages + pidx);
+    if (page < 0 || page >= p.num_pages) {
+      page_err = 1;
+      page = -1;
+    }
+    return page;
+  }
+
+  // Emit the prefix tiles [t0, t1) of a decode/paged stream, keys 0..P-1 of
+  // sequence b, KV head g.  Page-table entries for 8 tiles are fetched at once.
+  __device__ void emit_pool_tiles_contig(int b, int g, int P, int t0, int t1) {
+    for (int tg = t0; tg < t1 && ok; tg += 8) {
+      // lane i: chunk i%4 of tile tg + i/4
+      const int t = tg + (lane >> 2);
+      const int k = t * kTileKeys + (lane & 3) * kChunkKeys;
+      int coord = p.pool_rows;  // out of range -> zero fill
+      if (t < t1 && k < P) {
+        const int page = page_of(b, k);
+        if (page >= 0) coord = (page * p.Hkv + g) * p.S + (k % p.S);
+      }
+      const int ntile = min(8, t1 - tg);
+      for (int j = 0; j < ntile && ok; ++j) {
+        int cd[4], ko[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cd[i] = __shfl_sync(0xffffffffu, coord, 4 * j + i);
+        const int tt = tg + j;
+        const int nvalid = min(kTileKeys, P - tt * kTileKeys);
+        emit_tile(0, nvalid == kTileKeys, nvalid, g, 0, tt * kTileKeys, cd, ko);
+      }
+    }
+  }
+
+  // Dense tiles: keys are rows [r0, r0+n) of a dense [tokens, Hkv, d] tensor
+  // starting at token coordinate tok0; key i has position kbase + i (kmode 0)
+  // or live_pos[kbase + i] (kmode 2).  `min_lim` decides fully-included tiles
+  // when positions are contiguous.
+  __device__ void emit_dense_tile(int g, int tok0, int nvalid, int kmode, int kbase, int full) {
+    int cd[4], ko[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cd[i] = (i * kChunkKeys < nvalid) ? tok0 + i * kChunkKeys : p.dense_tokens;
+    emit_tile(1, full, nvalid, g, kmode, kbase, cd, ko);
+  }
+
+  // --------------------------------------------------------------------------
+  __device__ int decode_prefix(int b, int* bad) const {
+    const int P = __ldg(p.lens + b);
+    const long long cap = (long long)p.max_pages * p.S;
+    if (P < 0 || P % p.Dblk != 0 || (long long)P + p.Dblk > cap) {
+      *bad = 1;
+      return 0;
+    }
+    return P;
+  }
+  __device__ int decode_tiles(int P) const {
+    return ceil_div(P, kTileKeys) + ceil_div(p.Dblk, kTileKeys);
+  }
+
+  __device__ void run_decode() {
+    const int B = p.B, D = p.Dblk;
+    const int per_seq = p.Hkv * p.n_rb;
+    int bad = 0;
+    long long tot = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      if (b < B) tot += decode_tiles(decode_prefix(b, &bad));
+    }
+    tot = warp_sum_ll(tot) * per_seq;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, kErrBadLength);
+    const long long target = (long long)gridDim.x * max(1, p.waves);
+    long long ch = (tot + target - 1) / target;
+    int CH = (int)(ch > (long long)max(1, p.ch_min) ? ch : (long long)max(1, p.ch_min));
+    // respect the split workspace capacity
+    for (int guard = 0; guard < 40; ++guard) {
+      long long ns = 0;
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        const int b = b0 + lane;
+        if (b < B) {
+          int dummy = 0;
+          const int nch = ceil_div(decode_tiles(decode_prefix(b, &dummy)), CH);
+          if (nch > 1) ns += nch;
+        }
+      }
+      ns = warp_sum_ll(ns) * per_seq;
+      if (ns <= p.split_cap) break;
+      CH = CH > (1 << 29) ? CH : CH * 2;
+    }
+    if (blockIdx.x == 0 && lane == 0) p.hdr->chunk_tiles = CH;
+
+    long long next = blockIdx.x, item_off = 0, split_off = 0;
+    for (int b0 = 0; b0 < B && ok; b0 += 32) {
+      const int b = b0 + lane;
+      int P = 0, nt = 0, nch = 0;
+      long long items = 0, splits = 0;
+      if (b < B) {
+        int dummy = 0;
+        P = decode_prefix(b, &dummy);
+        nt = decode_tiles(P);
+        nch = ceil_div(nt, CH);
+        items = (long long)nch * per_seq;
+        splits = nch > 1 ? items : 0;
+      }
+      const long long exi = warp_excl_scan_ll(items, lane);
+      const long long exs = warp_excl_scan_ll(splits, lane);
+      const long long win_items = warp_sum_ll(items);
+      const long long win_splits = warp_sum_ll(splits);
+      if (blockIdx.x == 0 && b < B) p.split_base[b] = (int)(split_off + exs);
+      while (ok && next < item_off + win_items) {
+        const long long local = next - item_off;
+        const unsigned own = __ballot_sync(0xffffffffu, b < B && local >= exi && local < exi + items);
+        const int src = __ffs(own) - 1;
+        const int bo = b0 + src;
+        const int Po = __shfl_sync(0xffffffffu, P, src);
+        const int nto = __shfl_sync(0xffffffffu, nt, src);
+        const int ncho = __shfl_sync(0xffffffffu, nch, src);
+        const long long exio = __shfl_sync(0xffffffffu, exi, src);
+        const long long exso = __shfl_sync(0xffffffffu, exs, src);
+        const long long l2 = local - exio;
+        const int cidx = (int)(l2 % ncho);
+        const long long rest = l2 / ncho;
+        const int rb = (int)(rest % p.n_rb);
+        const int g = (int)(rest / p.n_rb);
+        const int split = ncho > 1 ? (int)(split_off + exso + l2) : -1;
+        const int t0 = cidx * CH, t1 = min(nto, t0 + CH);
+        decode_item(bo, Po, g, rb, t0, t1, split);
+        next += gridDim.x;
+      }
+      item_off += win_items;
+      split_off += win_splits;
+    }
+  }
+
+  __device__ void decode_item(int b, int P, int g, int rb, int t0, int t1, int split) {
+    const int D = p.Dblk;
+    int qtok[2], qhead[2], ntok[2], qbase[2];
+    for (int m = 0; m < 2; ++m) {
+      const int tok = rb * 2 * p.tpm + m * p.tpm;
+      ntok[m] = max(0, min(p.tpm, D - tok));
+      qtok[m] = b * D + tok;
+      qhead[m] = g * p.G;
+      qbase[m] = P + tok;
+    }
+    const int n_m = ntok[1] > 0 ? 2 : 1;
+    emit_item(t1 - t0, n_m, 0, qtok, qhead, ntok, qbase, P, D, split);
+    const int n_pre = ceil_div(P, kTileKeys);
+    // prefix tiles through the page table
+    if (t0 < n_pre) emit_pool_tiles_contig(b, g, P, t0, min(t1, n_pre));
+    // the block's own keys, dense
+    for (int t = max(t0, n_pre); t < t1 && ok; ++t) {
+      const int o = (t - n_pre) * kTileKeys;
+      const int nvalid = min(kTileKeys, D - o);
+      emit_dense_tile(g, b * D + o, nvalid, 0, P + o, nvalid == kTileKeys);
+    }
+  }
+
+  // --------------------------------------------------------------------------
+  __device__ void run_prefill() {
+    const int B = p.B, D = p.Dblk;
+    const int per_qt = p.Hkv * p.n_hp;
+    long long next = blockIdx.x, item_off = 0;
+    int bad = 0;
+    for (int b0 = 0; b0 < B && ok; b0 += 32) {
+      const int b = b0 + lane;
+      int start = 0, T = 0;
+      long long items = 0;
+      if (b < B) {
+        start = __ldg(p.lens + b);
+        const int end = __ldg(p.lens + b + 1);
+        T = end - start;
+        if (start < 0 || T < 0 || end > p.dense_tokens) {
+          bad = 1;
+          T = 0;
+        }
+        items = (long long)ceil_div(T, kRowsPerMTile) * per_qt;
+      }
+      const long long exi = warp_excl_scan_ll(items, lane);
+      const long long win_items = warp_sum_ll(items);
+      while (ok && next < item_off + win_items) {
+        const long long local = next - item_off;
+        const unsigned own = __ballot_sync(0xffffffffu, b < B && local >= exi && local < exi + items);
+        const int src = __ffs(own) - 1;
+        const int so = __shfl_sync(0xffffffffu, start, src);
+        const int To = __shfl_sync(0xffffffffu, T, src);
+        const long long l2 = local - __shfl_sync(0xffffffffu, exi, src);
+        const int n_qt = ceil_div(To, kRowsPerMTile);
+        const int qt = n_qt - 1 - (int)(l2 / per_qt);  // longest rows first
+        const int rest = (int)(l2 % per_qt);
+        const int g = rest / p.n_hp, hp = rest % p.n_hp;
+        prefill_item(so, To, qt, g, hp, D);
+        next += gridDim.x;
+      }
+      item_off += win_items;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, kErrBadLength);
+  }
+
+  __device__ void prefill_item(int start, int T, int qt, int g, int hp, int D) {
+    const int q0 = qt * kRowsPerMTile;
+    const int nq = min(kRowsPerMTile, T - q0);
+    const int min_lim = min(row_limit(q0, 0, D), T);
+    const int max_lim = min(row_limit(q0 + nq - 1, 0, D), T);
+    const int n_tiles = ceil_div(max_lim, kTileKeys);
+    int qtok[2], qhead[2], ntok[2], qbase[2];
+    const int h0 = 2 * hp;
+    for (int m = 0; m < 2; ++m) {
+      qtok[m] = start + q0;
+      qhead[m] = g * p.G + h0 + m;
+      ntok[m] = (h0 + m < p.G) ? nq : 0;
+      qbase[m] = q0;
+    }
+    const int n_m = ntok[1] > 0 ? 2 : 1;
+    emit_item(n_tiles, n_m, 0, qtok, qhead, ntok, qbase, 0, D, -1);
+    n_skip += (unsigned long long)(ceil_div(T, kTileKeys) - n_tiles);
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      const int k0 = t * kTileKeys;
+      const int nvalid = min(kTileKeys, T - k0);
+      const int full = (nvalid == kTileKeys) && (k0 + kTileKeys - 1 < min_lim);
+      emit_dense_tile(g, start + k0, nvalid, 0, k0, full);
+    }
+  }
+
+  // --------------------------------------------------------------------------
+  __device__ int live_position(int b, int r) const {
+    return p.live_pos ? __ldg(p.live_pos + (size_t)b * p.max_live + r) : p.prompt_len + r;
+  }
+
+  __device__ void run_multicanvas() {
+    const int B = p.B;
+    const int rows_per_item = 2 * p.tpm;
+    long long next = blockIdx.x, item_off = 0;
+    int bad = 0;
+    for (int b0 = 0; b0 < B && ok; b0 += 32) {
+      const int b = b0 + lane;
+      int n_live = 0, A = 0;
+      long long items = 0;
+      if (b < B) {
+        n_live = p.lens ? __ldg(p.lens + b) : p.max_live;
+        A = __ldg(p.arena_len + b);
+        if (n_live < 0 || n_live > p.max_live || A < 0 || (long long)A > (long long)p.max_pages * p.S) {
+          bad = 1;
+          n_live = 0;
+          A = 0;
+        }
+        items = (long long)ceil_div(n_live, rows_per_item) * p.Hkv;
+      }
+      const long long exi = warp_excl_scan_ll(items, lane);
+      const long long win_items = warp_sum_ll(items);
+      while (ok && next < item_off + win_items) {
+        const long long local = next - item_off;
+        const unsigned own = __ballot_sync(0xffffffffu, b < B && local >= exi && local < exi + items);
+        const int src = __ffs(own) - 1;
+        const int bo = b0 + src;
+        const int nlo = __shfl_sync(0xffffffffu, n_live, src);
+        const int Ao = __shfl_sync(0xffffffffu, A, src);
+        const long long l2 = local - __shfl_sync(0xffffffffu, exi, src);
+        const int rb = (int)(l2 / p.Hkv), g = (int)(l2 % p.Hkv);
+        multicanvas_item(bo, nlo, Ao, g, rb);
+        next += gridDim.x;
+      }
+      item_off += win_items;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, kErrBadLength);
+  }
+
+  // Classify one arena tile (entries [64a, 64a+64) of sequence b):
+  // returns 0 skip, 1 partial, 2 full; fills coords/offsets on lane 0.
+  __device__ int arena_tile(int b, int A, int a, int g, int min_lim, int max_lim, int (&cd)[4],
+                            int (&ko)[4]) {
+    int kmin = INT_MAX, kmax = INT_MIN, pg[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = a * kTileKeys + 32 * h + lane;
+      pg[h] = -1;
+      if (e < A) {
+        const int page = page_of(b, e);
+        pg[h] = page;
+        if (page >= 0) {
+          const int pos = __ldg(p.kv_pos + (size_t)page * p.S + (e % p.S));
+          kmin = min(kmin, pos);
+          kmax = max(kmax, pos);
+        }
+      }
+    }
+    kmin = warp_min(kmin);
+    kmax = warp_max(kmax);
+    const int nvalid = min(kTileKeys, A - a * kTileKeys);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // chunk i starts at entry 16i: lane 16*(i&1) of load half i>>1
+      const int page = __shfl_sync(0xffffffffu, (i >> 1) ? pg[1] : pg[0], 16 * (i & 1));
+      const int e = a * kTileKeys + i * kChunkKeys;
+      cd[i] = (e < A && page >= 0) ? (page * p.Hkv + g) * p.S + (e % p.S) : p.pool_rows;
+      ko[i] = (e < A && page >= 0) ? page * p.S + (e % p.S) : 0;
+    }
+    if (kmin >= max_lim) return 0;
+    if (kmax < min_lim && nvalid == kTileKeys) return 2;
+    return 1;
+  }
+
+  __device__ int live_tile(int b, int n_live, int l, int min_lim, int max_lim) {
+    int kmin = INT_MAX, kmax = INT_MIN;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = l * kTileKeys + 32 * h + lane;
+      if (r < n_live) {
+        const int pos = live_position(b, r);
+        kmin = min(kmin, pos);
+        kmax = max(kmax, pos);
+      }
+    }
+    kmin = warp_min(kmin);
+    kmax = warp_max(kmax);
+    const int nvalid = min(kTileKeys, n_live - l * kTileKeys);
+    if (kmin >= max_lim) return 0;
+    if (kmax < min_lim && nvalid == kTileKeys) return 2;
+    return 1;
+  }
+
+  __device__ void multicanvas_item(int b, int n_live, int A, int g, int rb) {
+    const int r0 = rb * 2 * p.tpm;
+    const int nrows = min(2 * p.tpm, n_live - r0);
+    int lo = INT_MAX, hi = INT_MIN;
+    for (int r = lane; r < nrows; r += 32) {
+      const int lim = row_limit(live_position(b, r0 + r), p.prompt_len, p.Dblk);
+      lo = min(lo, lim);
+      hi = max(hi, lim);
+    }
+    const int min_lim = warp_min(lo), max_lim = warp_max(hi);
+    const int n_at = ceil_div(A, kTileKeys), n_lt = ceil_div(n_live, kTileKeys);
+    // pass 1: count the tiles that are not fully excluded
+    int n_tiles = 0;
+    for (int a = 0; a < n_at; ++a) {
+      int cd[4], ko[4];
+      if (arena_tile(b, A, a, g, min_lim, max_lim, cd, ko) != 0) ++n_tiles;
+    }
+    for (int l = 0; l < n_lt; ++l)
+      if (live_tile(b, n_live, l, min_lim, max_lim) != 0) ++n_tiles;
+    int qtok[2], qhead[2], ntok[2], qbase[2];
+    for (int m = 0; m < 2; ++m) {
+      const int r = r0 + m * p.tpm;
+      ntok[m] = max(0, min(p.tpm, n_live - r));
+      qtok[m] = b * p.max_live + r;
+      qhead[m] = g * p.G;
+      qbase[m] = p.live_pos ? b * p.max_live + r : p.prompt_len + r;
+    }
+    const int n_m = ntok[1] > 0 ? 2 : 1;
+    emit_item(n_tiles, n_m, p.live_pos ? 1 : 0, qtok, qhead, ntok, qbase, p.prompt_len, p.Dblk,
+              -1);
+    n_skip += (unsigned long long)(n_at + n_lt - n_tiles);
+    // pass 2: emit
+    for (int a = 0; a < n_at && ok; ++a) {
+      int cd[4], ko[4];
+      const int cls = arena_tile(b, A, a, g, min_lim, max_lim, cd, ko);
+      if (cls == 0) continue;
+      emit_tile(0, cls == 2, min(kTileKeys, A - a * kTileKeys), g, 1, 0, cd, ko);
+    }
+    for (int l = 0; l < n_lt && ok; ++l) {
+      const int cls = live_tile(b, n_live, l, min_lim, max_lim);
+      if (cls == 0) continue;
+      const int nvalid = min(kTileKeys, n_live - l * kTileKeys);
+      const int kmode = p.live_pos ? 2 : 0;
+      const int kbase = p.live_pos ? b * p.max_live + l * kTileKeys : p.prompt_len + l * kTileKeys;
+      emit_dense_tile(g, b * p.max_live + l * kTileKeys, nvalid, kmode, kbase, cls == 2);
+    }
+  }
+
+  __device__ void run() {
+    if (p.mode == kModeDecode) run_decode();
+    else if (p.mode == kModePrefill) run_prefill();
+    else run_multicanvas();
+    if (ok) emit_end();
+    if (__any_sync(0xffffffffu, page_err) && lane == 0) record_error(p, kErrPageOob);
+    if (lane == 0) {
+      if (n_full) atomicAdd(&p.hdr->tiles_full, n_full);
+      if (n_partial) atomicAdd(&p.hdr->tiles_partial, n_partial);
+      if (n_skip) atomicAdd(&p.hdr->tiles_skipped, n_skip);
+    }
+  }
+};
+
+// Consumer side of the record ring (whole-warp roles).
+__device__ __forceinline__ const Rec* ring_get(const Ctx& c, const AttnParams& p, uint32_t i) {
+  if (!wait_bar_warp(c, p, &c.bar.rec_full[i % kNumRec], (i / kNumRec) & 1)) return nullptr;
+  return &c.ring[i % kNumRec];
+}
+__device__ __forceinline__ void ring_release(const Ctx& c, uint32_t i, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&c.bar.rec_empty[i % kNumRec]);
+}
+// Single-thread role (the MMA issuer).
+__device__ __forceinline__ const Rec* ring_get1(const Ctx& c, const AttnParams& p, uint32_t i) {
+  if (!wait_bar(c, p, &c.bar.rec_full[i % kNumRec], (i / kNumRec) & 1)) return nullptr;
+  return &c.ring[i % kNumRec];
+}
+__device__ __forceinline__ void ring_release1(const Ctx& c, uint32_t i) {
+  mbar_arrive(&c.bar.rec_empty[i % kNumRec]);
+}
+
+// ============================================================================
+// loader (warp 0)
+// ============================================================================
+template <int HD>
+__device__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap* tm_q,
+                           const CUtensorMap* tm_kp, const CUtensorMap* tm_vp,
+                           const CUtensorMap* tm_kd, const CUtensorMap* tm_vd, int lane) {
+  using C = Cfg<HD>;
+  const uint32_t q_base = smem_u32(c.smem + C::kOffQ);
+  const uint32_t kv_base = smem_u32(c.smem + C::kOffKV);
+  uint32_t ri = 0, u = 0, qn[2] = {0, 0};
+  bool ok = true;
+  while (ok) {
+    const Rec* r = ring_get(c, p, ri);
+    if (!r) break;
+    const int kind = r->w[0];
+    int f[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = r->w[i];
+    ring_release(c, ri, lane);
+    ++ri;
+    if (kind == kRecEnd) break;
+    if (kind == kRecItem) {
+      const int n_m = f[I_NM];
+      for (int m = 0; m < n_m; ++m) {
+        if (!wait_bar_warp(c, p, &c.bar.q_empty[m], (qn[m] & 1) ^ 1)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&c.bar.q_full[m], C::kQBytes);
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(q_base + m * C::kQBytes + h * 16384, tm_q, &c.bar.q_full[m], h * 64,
+                        f[I_QHEAD + m], f[I_QTOK + m]);
+        }
+        __syncwarp();
+        ++qn[m];
+      }
+      continue;
+    }
+    // a KV tile: K then V, each into the next stage
+    const int src = f[T_SRC], nvalid = f[T_NVALID], head = f[T_HEAD];
+    for (int kv = 0; kv < 2 && ok; ++kv) {
+      const uint32_t slot = u % C::kStages;
+      if (!wait_bar_warp(c, p, &c.bar.kv_empty[slot], ((u / C::kStages) & 1) ^ 1)) { ok = false; break; }
+      const uint32_t dst = kv_base + slot * C::kSlotBytes;
+      uint32_t tma_bytes = 0;
+      bool manual = false;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int nv = min(max(nvalid - i * kChunkKeys, 0), kChunkKeys);
+        if (nv == 0 || nv == kChunkKeys) {
+          tma_bytes += C::kHalves * 2048;
+          continue;
+        }
+        // ragged chunk: copy the valid rows with the warp, zero the rest
+        manual = true;
+        const uint16_t* base = src == 0 ? (kv ? p.v_pool : p.k_pool) : (kv ? p.v_dense : p.k_dense);
+        const int coord = f[T_COORD + i];
+        for (int piece = lane; piece < kChunkKeys * C::kHalves * 8; piece += 32) {
+          const int rr = piece / (C::kHalves * 8);
+          const int h = (piece / 8) % C::kHalves;
+          const int cc = piece % 8;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (rr < nv) {
+            const size_t row = src == 0 ? (size_t)(coord + rr)
+                                        : (size_t)(coord + rr) * p.Hkv + head;
+            v = __ldg(reinterpret_cast<const uint4*>(base + row * HD + h * 64 + cc * 8));
+          }
+          const int krow = i * kChunkKeys + rr;
+          st_shared_v4(dst + h * 8192 + krow * 128 + ((cc ^ (krow & 7)) << 4), v.x, v.y, v.z, v.w);
+        }
+      }
+      if (manual) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (tma_bytes) mbar_arrive_expect_tx(&c.bar.kv_full[slot], tma_bytes);
+        else mbar_arrive(&c.bar.kv_full[slot]);
+        const CUtensorMap* map = src == 0 ? (kv ? tm_vp : tm_kp) : (kv ? tm_vd : tm_kd);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nv = min(max(nvalid - i * kChunkKeys, 0), kChunkKeys);
+          if (nv != 0 && nv != kChunkKeys) continue;
+          const int coord = f[T_COORD + i];  // planner made it out of range if nv == 0
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            const uint32_t d = dst + h * 8192 + i * 2048;
+            if (src == 0) tma_load_2d(d, map, &c.bar.kv_full[slot], h * 64, coord);
+            else tma_load_3d(d, map, &c.bar.kv_full[slot], h * 64, head, coord);
+          }
+        }
+      }
+      __syncwarp();
+      ++u;
+    }
+  }
+  // teardown: never leave this CTA with copies in flight
+  for (uint32_t k = 0; k < (uint32_t)C::kStages && k < u; ++k) {
+    const uint32_t uu = u - 1 - k;
+    mbar_wait(&c.bar.kv_full[uu % C::kStages], (uu / C::kStages) & 1, c.abort_flag, kWaitTimeoutNs);
+  }
+  for (int m = 0; m < 2; ++m)
+    if (qn[m]) mbar_wait(&c.bar.q_full[m], (qn[m] - 1) & 1, c.abort_flag, kWaitTimeoutNs);
+}
+
+// ============================================================================
+// MMA issuer (warp 1, one thread)
+// ============================================================================
+template <int HD>
+__device__ __forceinline__ void issue_qk(const Ctx& c, int m, uint32_t slot) {
+  using C = Cfg<HD>;
+  constexpr uint32_t idesc = make_idesc_bf16(128, kTileKeys, 0, 0);
+  const uint32_t qa = smem_u32(c.smem + C::kOffQ + m * C::kQBytes);
+  const uint32_t ka = smem_u32(c.smem + C::kOffKV + slot * C::kSlotBytes);
+  const uint32_t d = c.tmem + C::kColS + m * kTileKeys;
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    const int h = ks >> 2, kin = ks & 3;
+    const uint64_t a = make_sdesc_sw128(qa + h * 16384 + kin * 32, 16, 1024);
+    const uint64_t b = make_sdesc_sw128(ka + h * 8192 + kin * 32, 16, 1024);
+    umma_bf16(d, a, b, idesc, ks > 0 ? 1u : 0u);
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_pv(const Ctx& c, int m, uint32_t slot, bool acc) {
+  using C = Cfg<HD>;
+  constexpr uint32_t idesc = make_idesc_bf16(128, HD, 0, 1);
+  const uint32_t pa = smem_u32(c.smem + C::kOffP + m * C::kPBytes);
+  const uint32_t va = smem_u32(c.smem + C::kOffKV + slot * C::kSlotBytes);
+  const uint32_t d = c.tmem + C::kColO + m * HD;
+#pragma unroll
+  for (int ks = 0; ks < kTileKeys / 16; ++ks) {
+    const uint64_t a = make_sdesc_sw128(pa + ks * 32, 16, 1024);
+    const uint64_t b = make_sdesc_sw128(va + ks * 2048, 8192, 1024);
+    umma_bf16(d, a, b, idesc, (acc || ks > 0) ? 1u : 0u);
+  }
+}
+
+template <int HD>
+__device__ void run_mma(const Ctx& c, const AttnParams& p, int lane) {
+  using C = Cfg<HD>;
+  uint32_t ri = 0, u = 0, qn[2] = {0, 0}, pn[2] = {0, 0}, on[2] = {0, 0};
+  bool ok = true;
+  while (ok) {
+    const Rec* r = ring_get1(c, p, ri);
+    if (!r) break;
+    const int kind = r->w[I_KIND], n_t = r->w[I_NT], n_m = r->w[I_NM];
+    ring_release1(c, ri);
+    ++ri;
+    if (kind == kRecEnd) break;
+    // kind == item
+    for (int m = 0; m < n_m && ok; ++m) {
+      ok = wait_bar(c, p, &c.bar.q_full[m], qn[m] & 1);
+      ++qn[m];
+    }
+    if (!ok) break;
+    tc_fence_after();
+    // tile 0: S = Q K^T for every active M-tile
+    if (!ring_get1(c, p, ri)) break;
+    ring_release1(c, ri);
+    ++ri;
+    uint32_t ks = u % C::kStages;
+    if (!wait_bar(c, p, &c.bar.kv_full[ks], (u / C::kStages) & 1)) break;
+    ++u;
+    tc_fence_after();
+    for (int m = 0; m < n_m; ++m) {
+      issue_qk<HD>(c, m, ks);
+      umma_commit(&c.bar.s_full[m]);
+      if (n_t == 1) umma_commit(&c.bar.q_empty[m]);
+    }
+    umma_commit(&c.bar.kv_empty[ks]);
+    for (int j = 0; j < n_t && ok; ++j) {
+      const uint32_t vs = u % C::kStages;
+      if (!(ok = wait_bar(c, p, &c.bar.kv_full[vs], (u / C::kStages) & 1))) break;
+      ++u;
+      tc_fence_after();
+      const bool nxt = j + 1 < n_t;
+      if (nxt) {
+        if (!(ok = ring_get1(c, p, ri) != nullptr)) break;
+        ring_release1(c, ri);
+        ++ri;
+      }
+      for (int m = 0; m < n_m && ok; ++m) {
+        if (!(ok = wait_bar(c, p, &c.bar.p_full[m], pn[m] & 1))) break;
+        ++pn[m];
+        if (j == 0) {
+          if (!(ok = wait_bar(c, p, &c.bar.o_empty[m], (on[m] & 1) ^ 1))) break;
+        }
+        tc_fence_after();
+        issue_pv<HD>(c, m, vs, j > 0);
+        if (m == n_m - 1) umma_commit(&c.bar.kv_empty[vs]);
+        if (nxt) {
+          if (m == 0) {
+            ks = u % C::kStages;
+            if (!(ok = wait_bar(c, p, &c.bar.kv_full[ks], (u / C::kStages) & 1))) break;
+            ++u;
+            tc_fence_after();
+          }
+          issue_qk<HD>(c, m, ks);
+          umma_commit(&c.bar.s_full[m]);
+          if (j + 2 == n_t) umma_commit(&c.bar.q_empty[m]);
+          if (m == n_m - 1) umma_commit(&c.bar.kv_empty[ks]);
+        } else {
+          umma_commit(&c.bar.o_full[m]);
+          ++on[m];
+        }
+      }
+    }
+  }
+  // teardown: wait until every MMA issued by this thread has completed
+  umma_commit(c.bar.drain);
+  mbar_wait(c.bar.drain, 0, c.abort_flag, kWaitTimeoutNs);
+}
+
+// ============================================================================
+// softmax / epilogue (warps 4..11)
+// ============================================================================
+template <int HD>
+__device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, int lane) {
+  using C = Cfg<HD>;
+  const int r = 32 * wq + lane;  // row within the M-tile == TMEM lane
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * wq) << 16;
+  const uint32_t t_s = c.tmem + lane_addr + C::kColS + m * kTileKeys;
+  const uint32_t t_o = c.tmem + lane_addr + C::kColO + m * HD;
+  const uint32_t p_row = smem_u32(c.smem + C::kOffP + m * C::kPBytes) + r * 128;
+  const uint32_t sw = r & 7;
+  uint32_t ri = 0, sn = 0, on = 0;
+  while (true) {
+    const Rec* rec = ring_get(c, p, ri);
+    if (!rec) return;
+    const int kind = rec->w[I_KIND];
+    const int n_t = rec->w[I_NT], n_m = rec->w[I_NM], qmode = rec->w[I_QMODE];
+    const int qtok = rec->w[I_QTOK + m], qhead = rec->w[I_QHEAD + m];
+    const int ntok = rec->w[I_NTOK + m], qbase = rec->w[I_QBASE + m];
+    const int P0 = rec->w[I_P0], Dblk = rec->w[I_DBLK], split = rec->w[I_SPLIT];
+    ring_release(c, ri, lane);
+    ++ri;
+    if (kind == kRecEnd) return;
+    const bool active = m < n_m;
+    const int tok = r / p.hpr;
+    const bool valid = active && r < p.hpr * p.tpm && tok < ntok;
+    int lim = INT_MAX;
+    if (valid) {
+      const int qpos = qmode == 0 ? qbase + tok : __ldg(p.live_pos + qbase + tok);
+      lim = row_limit(qpos, P0, Dblk);
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < n_t; ++j) {
+      const Rec* t = ring_get(c, p, ri);
+      if (!t) return;
+      const int full = t->w[T_FULL], nvalid = t->w[T_NVALID], kmode = t->w[T_KMODE];
+      const int kbase = t->w[T_KBASE];
+      int koff[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) koff[i] = t->w[T_KOFF + i];
+      ring_release(c, ri, lane);
+      ++ri;
+      if (!active) continue;
+      if (!wait_bar_warp(c, p, &c.bar.s_full[m], sn & 1)) return;
+      ++sn;
+      tc_fence_after();
+      uint32_t s0[32], s1[32];
+      tmem_ld64_sync(t_s, s0, s1);
+      float x[64];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        x[k] = __uint_as_float(s0[k]) * p.scale_log2;
+        x[k + 32] = __uint_as_float(s1[k]) * p.scale_log2;
+      }
+      if (!full) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          int kp = INT_MAX;
+          if (k < nvalid) {
+            if (kmode == 0) kp = kbase + k;
+            else if (kmode == 1) kp = __ldg(p.kv_pos + koff[k >> 4] + (k & 15));
+            else kp = __ldg(p.live_pos + kbase + k);
+          }
+          if (!(kp < lim)) x[k] = -INFINITY;
+        }
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int k = 1; k < 64; ++k) mt = fmaxf(mt, x[k]);
+      const float m_new = fmaxf(m_run, mt);
+      if (j == 0) {
+        m_run = m_new;
+      } else {
+        const bool need = m_new > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          // O holds the PV products of earlier tiles (complete: the S commit
+          // of this tile was issued after them); rescale it in TMEM.
+          const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32_sync(t_o + c0, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(t_o + c0, o);
+          }
+          tmem_st_wait();
+          l_run *= alpha;
+          if (need) m_run = m_new;
+        }
+      }
+      const float ref = m_run == -INFINITY ? 0.f : m_run;
+      float sum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = ex2_approx(x[8 * cc + 2 * k] - ref);
+          const float p1 = ex2_approx(x[8 * cc + 2 * k + 1] - ref);
+          sum += p0 + p1;
+          w[k] = pack_bf16x2(p0, p1);
+        }
+        st_shared_v4(p_row + ((cc ^ sw) << 4), w[0], w[1], w[2], w[3]);
+      }
+      l_run += sum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.bar.p_full[m]);
+    }
+    if (!active) continue;
+    if (!wait_bar_warp(c, p, &c.bar.o_full[m], on & 1)) return;
+    ++on;
+    tc_fence_after();
+    if (split < 0) {
+      const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      uint16_t* dst = p.out + ((size_t)(qtok + tok) * p.Hq + qhead + (r % p.hpr)) * HD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32_sync(t_o + c0, o);
+        if (valid) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c0 + 8 * k) = v;
+          }
+        }
+      }
+    } else {
+      const int R = m * kRowsPerMTile + r;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32_sync(t_o + c0, o);
+        if (valid) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float4 v = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                   __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+            const size_t idx = (((size_t)split * (HD / 4) + (c0 / 4 + k)) * 256 + R) * 4;
+            *reinterpret_cast<float4*>(p.part_o + idx) = v;
+          }
+        }
+      }
+      if (valid) {
+        *reinterpret_cast<float2*>(p.part_ml + ((size_t)split * 256 + R) * 2) =
+            make_float2(m_run, l_run);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.bar.o_empty[m]);
+  }
+}
+
+// ============================================================================
+// the kernel
+// ============================================================================
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_kp,
+                     const __grid_constant__ CUtensorMap tm_vp,
+                     const __grid_constant__ CUtensorMap tm_kd,
+                     const __grid_constant__ CUtensorMap tm_vd,
+                     const __grid_constant__ AttnParams p) {
+  using C = Cfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  Ctx c;
+  c.smem = smem;
+  c.ring = reinterpret_cast<Rec*>(smem + C::kOffRec);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  c.bar.rec_full = bars;
+  c.bar.rec_empty = bars + kNumRec;
+  c.bar.kv_full = bars + 2 * kNumRec;
+  c.bar.kv_empty = c.bar.kv_full + C::kStages;
+  c.bar.q_full = c.bar.kv_empty + C::kStages;
+  c.bar.q_empty = c.bar.q_full + 2;
+  c.bar.s_full = c.bar.q_empty + 2;
+  c.bar.p_full = c.bar.s_full + 2;
+  c.bar.o_full = c.bar.p_full + 2;
+  c.bar.o_empty = c.bar.o_full + 2;
+  c.bar.drain = c.bar.o_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  c.abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumRec; ++i) {
+      mbar_init(&c.bar.rec_full[i], 1);
+      mbar_init(&c.bar.rec_empty[i], kRecConsumers);
+    }
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&c.bar.kv_full[i], 1);
+      mbar_init(&c.bar.kv_empty[i], 1);
+    }
+    for (int m = 0; m < 2; ++m) {
+      mbar_init(&c.bar.q_full[m], 1);
+      mbar_init(&c.bar.q_empty[m], 1);
+      mbar_init(&c.bar.s_full[m], 1);
+      mbar_init(&c.bar.p_full[m], 4);
+      mbar_init(&c.bar.o_full[m], 1);
+      mbar_init(&c.bar.o_empty[m], 4);
+    }
+    mbar_init(c.bar.drain, 1);
+    *c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kp);
+    tma_prefetch_desc(&tm_vp);
+    tma_prefetch_desc(&tm_kd);
+    tma_prefetch_desc(&tm_vd);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  c.tmem = *tmem_slot;
+
+  if (warp == 3) {
+    Planner pl(p, c, lane);
+    pl.run();
+  } else if (warp == 0) {
+    run_loader<HD>(c, p, &tm_q, &tm_kp, &tm_vp, &tm_kd, &tm_vd, lane);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<HD>(c, p, lane);
+  } else if (warp >= 4) {
+    run_softmax<HD>(c, p, (warp - 4) >> 2, warp & 3, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(c.tmem, C::kTmemCols);
+  }
+}
+
+// ============================================================================
+// split-KV combine (decode): O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c
+// ============================================================================
+template <int HD>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p) {
+  const int per_b = p.Hkv * p.n_rb;
+  const int b = blockIdx.x / per_b;
+  const int rem = blockIdx.x % per_b;
+  const int g = rem / p.n_rb, rb = rem % p.n_rb;
+  const int D = p.Dblk;
+  int P = __ldg(p.lens + b);
+  if (P < 0 || P % D != 0 || (long long)P + D > (long long)p.max_pages * p.S) P = 0;
+  const int nt = ceil_div(P, kTileKeys) + ceil_div(D, kTileKeys);
+  const int CH = p.hdr->chunk_tiles;
+  const int nch = ceil_div(nt, CH);
+  if (nch <= 1) return;
+  const int R = threadIdx.x;
+  const int m = R / kRowsPerMTile, r = R % kRowsPerMTile;
+  const int tok = rb * 2 * p.tpm + m * p.tpm + r / p.hpr;
+  if (r >= p.hpr * p.tpm || tok >= D) return;
+  const int base = p.split_base[b] + (g * p.n_rb + rb) * nch;
+  float M = -INFINITY;
+  for (int ci = 0; ci < nch; ++ci) M = fmaxf(M, p.part_ml[((size_t)(base + ci) * 256 + R) * 2]);
+  float acc[HD];
+#pragma unroll
+  for (int k = 0; k < HD; ++k) acc[k] = 0.f;
+  float den = 0.f;
+  for (int ci = 0; ci < nch; ++ci) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((size_t)(base + ci) * 256 + R) * 2);
+    const float w = ml.x == -INFINITY ? 0.f : ex2_approx(ml.x - M);
+    den += w * ml.y;
+#pragma unroll
+    for (int k4 = 0; k4 < HD / 4; ++k4) {
+      const float4 v = *reinterpret_cast<const float4*>(
+          p.part_o + (((size_t)(base + ci) * (HD / 4) + k4) * 256 + R) * 4);
+      acc[4 * k4 + 0] += w * v.x;
+      acc[4 * k4 + 1] += w * v.y;
+      acc[4 * k4 + 2] += w * v.z;
+      acc[4 * k4 + 3] += w * v.w;
+    }
+  }
+  const float inv = den > 0.f ? 1.0f / den : 0.f;
+  uint16_t* dst = p.out + ((size_t)(b * D + tok) * p.Hq + g * p.G + (r % p.hpr)) * HD;
+#pragma unroll
+  for (int k = 0; k < HD; k += 8) {
+    uint4 v;
+    v.x = pack_bf16x2(acc[k + 0] * inv, acc[k + 1] * inv);
+    v.y = pack_bf16x2(acc[k + 2] * inv, acc[k + 3] * inv);
+    v.z = pack_bf16x2(acc[k + 4] * inv, acc[k + 5] * inv);
+    v.w = pack_bf16x2(acc[k + 6] * inv, acc[k + 7] * inv);
+    *reinterpret_cast<uint4*>(dst + k) = v;
+  }
+}
+
+template <int HD>
+cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int grid,
+                                cudaStream_t stream) {
+  using C = Cfg<HD>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  attention_kernel<HD><<<grid, kThreads, C::kSmemAlloc, stream>>>(maps.q, maps.kp, maps.vp,
+                                                                  maps.kd, maps.vd, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head_dim, int grid,
+                             cudaStream_t stream) {
+  if (head_dim == 128) return launch_attention_hd<128>(p, maps, grid, stream);
+  return launch_attention_hd<64>(p, maps, grid, stream);
+}
+
+cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, cudaStream_t stream) {
+  const int blocks = p.B * p.Hkv * p.n_rb;
+  if (blocks == 0) return cudaSuccess;
+  if (head_dim == 128) combine_kernel<128><<<blocks, 256, 0, stream>>>(p);
+  else combine_kernel<64><<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace bca

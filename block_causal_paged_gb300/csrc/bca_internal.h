@@ -1,0 +1,121 @@
+// Internal declarations shared by the host API and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bca {
+
+constexpr int kTileKeys = 64;     // keys per KV tile
+constexpr int kChunkKeys = 16;    // keys per TMA box (a page holds whole chunks)
+constexpr int kRowsPerMTile = 128;
+constexpr int kThreads = 384;     // 12 warps, see the role map in attention.cu
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s per internal wait
+
+enum Mode : int { kModeDecode = 0, kModePrefill = 1, kModeMulticanvas = 2 };
+
+// First 256 bytes of every workspace.
+struct WsHeader {
+  int32_t status;          // first device-detected error (0 = none)
+  int32_t chunk_tiles;     // decode: KV tiles per split chunk chosen by the planner
+  int32_t reserved0[2];
+  unsigned long long tiles_full;
+  unsigned long long tiles_partial;
+  unsigned long long tiles_skipped;
+  int32_t reserved1[54];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+constexpr size_t kWsHeaderBytes = 256;
+
+// Decode workspace: header | split_base int32[B] (256-aligned) | partial
+// (max, sum) float2[cap][256] | partial O float[cap][d/4][256][4].
+struct DecodeWsLayout {
+  size_t split_base_off, ml_off, o_off, bytes_per_slot;
+  int cap;
+};
+DecodeWsLayout decode_ws_layout(int B, int head_dim, size_t ws_bytes);
+size_t decode_ws_recommended(int B, int Hkv, int n_rb, int head_dim, int n_sms);
+
+struct AttnParams {
+  int mode;
+  int B, Hq, Hkv, G, S, num_pages, max_pages;
+  int Dblk;            // decode/prefill block size D, or canvas length C
+  int hpr, tpm;        // heads per row group and tokens per M-tile (hpr * tpm <= 128)
+  int n_hp;            // prefill: M-tile pairs (heads) per KV head
+  int n_rb;            // decode: row blocks per KV head (each = 2 M-tiles)
+  int ch_min, waves;   // decode split policy
+  float scale_log2;    // softmax scale * log2(e)
+  const int32_t* page_table;
+  const int32_t* lens;       // decode prefix_len | prefill cu_seqlens | multicanvas live_count
+  const int32_t* live_pos;   // multicanvas (may be null)
+  const int32_t* kv_pos;     // multicanvas arena positions [num_pages, S]
+  const int32_t* arena_len;  // multicanvas
+  int max_live, prompt_len;
+  const uint16_t* k_pool;
+  const uint16_t* v_pool;
+  const uint16_t* k_dense;   // decode k_blk | prefill k | multicanvas k_live
+  const uint16_t* v_dense;
+  int pool_rows;             // num_pages * Hkv * S
+  int dense_tokens;          // token rows of the dense K/V view
+  uint16_t* out;             // bf16 [q_tokens, Hq, d]
+  WsHeader* hdr;
+  int32_t* split_base;
+  float* part_ml;
+  float* part_o;
+  int split_cap;
+};
+
+struct AttnMaps {
+  CUtensorMap q, kp, vp, kd, vd;
+};
+
+// Launch the block-causal attention kernel (decode, prefill or multicanvas).
+cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head_dim, int grid,
+                             cudaStream_t stream);
+
+// Split-KV combine for decode (only sequences that were split do work).
+cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, cudaStream_t stream);
+
+// Bit copy of K/V rows into pages.  Source rows are [rows, Hkv, d]; sequence
+// b owns rows src_first(b) .. src_first(b)+count(b)-1 and writes them to
+// logical positions start(b) .. start(b)+count(b)-1 of its pages.
+//   cu != null (prefill): src_first = cu[b], count = cu[b+1]-cu[b], start = 0
+//   cu == null (commit):  src_first = b*rows_per_seq, count = num_tokens,
+//                         start = start_pos[b]
+struct CommitParams {
+  const uint16_t* k_src;
+  const uint16_t* v_src;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  const int32_t* page_table;
+  const int32_t* start_pos;
+  const int32_t* cu;
+  int rows_per_seq;
+  int num_tokens;
+  int max_rows;                 // host bound on count(b), for the grid
+  int B, Hkv, d, S, num_pages, max_pages;
+  WsHeader* hdr;
+};
+cudaError_t launch_commit(const CommitParams& c, cudaStream_t stream);
+
+// Arena promotion after a multicanvas step.
+struct PromoteParams {
+  const uint16_t* k_live;
+  const uint16_t* v_live;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  const int32_t* page_table;
+  const int32_t* live_pos;
+  const int32_t* live_count;
+  int32_t* kv_pos;
+  int32_t* arena_len;
+  const int32_t* commit_rows;
+  const int32_t* commit_count;
+  int B, Hkv, d, S, num_pages, max_pages, max_live, max_commit, prompt_len;
+  WsHeader* hdr;
+};
+cudaError_t launch_promote(const PromoteParams& c, cudaStream_t stream);
+
+}  // namespace bca

@@ -1,0 +1,243 @@
+/*
+ * bca.h -- block-causal paged attention on one GPU (sm_103a), C ABI.
+ *
+ * The operation is the attention of a text-diffusion decode step:
+ *
+ *   "Inference for Interpretable Text-Diffusion Models", section
+ *   "Background" (first bullet): a token attends bidirectionally to every
+ *   token of its own diffusion block, causally to tokens of earlier blocks,
+ *   and never to later blocks; completed blocks are therefore cacheable.
+ *   Sections "KV Cache" (prefill -> decode -> commit) and "Paged Attention"
+ *   (a page table maps logical positions to fixed-size physical pages).
+ *
+ *   "Inference: Fewer, smaller forwards", "Advancement 1" (block-causal
+ *   multi-canvas decode), "Advancement 9" (only live rows are queries),
+ *   "Advancement 10"/"Advancement 11" (keys carry their absolute position;
+ *   an arena of promoted rows) and "Advancement 13" (canvas c attends the
+ *   contiguous prefix of positions below the end of canvas c).
+ *
+ * Every position p gets a block index blk(p) = -1 if p < P0, else
+ * floor((p - P0) / D); a query at position i sees the key at position j iff
+ * blk(j) <= blk(i).  Scores are scale * q.k (scale defaults to 1/sqrt(d)),
+ * softmax over the visible keys, fp32 accumulation, bf16 output rounded to
+ * nearest even.  Query head h reads key/value head h / (Hq / Hkv).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; bf16
+ *    tensors are passed as void*.  Every pointer must be 16-byte aligned.
+ *  - Layouts (row-major, innermost last):
+ *      decode Q / out          [B, D, Hq, d]       k_blk, v_blk [B, D, Hkv, d]
+ *      K and V pools           [num_pages, Hkv, page_size, d] (separate tensors)
+ *      page_table (int32)      [B, max_pages_per_seq]; logical position p of
+ *                              sequence b lives in page page_table[b][p / S],
+ *                              slot p % S.  Entries that are never touched may
+ *                              hold anything (e.g. -1).
+ *  - The library never allocates, frees or synchronizes (except
+ *    bca_read_device_status).  Every call is asynchronous on `stream`
+ *    (a cudaStream_t; NULL = legacy default stream).  Launch arguments are
+ *    captured by value, so calls may be recorded into a CUDA graph.
+ *  - Host-detectable errors return a negative code before anything is
+ *    launched.  Errors that depend on device data (page ids, lengths) are
+ *    detected by the kernels, which then skip the offending tile or sequence
+ *    and record the first such error in the status word at the start of the
+ *    caller's workspace; no kernel traps.  Read it with
+ *    bca_read_device_status.
+ *  - Workspace: caller-owned device memory of at least
+ *    bca_workspace_size(dims, op) bytes, prepared once with
+ *    bca_workspace_init.  Calls on the same workspace must be ordered on
+ *    one stream (they share its scratch area).
+ *  - head_dim must be 64 or 128; page_size a multiple of 16 in [16, 256];
+ *    Hq a multiple of Hkv with Hq / Hkv <= 128; any block size D >= 1.
+ */
+#ifndef BCA_H_
+#define BCA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BCA_ABI_VERSION 1
+
+/* Status codes. */
+#define BCA_OK 0
+#define BCA_ERR_INVALID_ARG (-1)      /* bad dims or scalar argument */
+#define BCA_ERR_NULL (-2)             /* a required pointer is NULL */
+#define BCA_ERR_ALIGN (-3)            /* a pointer is not 16-byte aligned */
+#define BCA_ERR_WORKSPACE (-4)        /* workspace NULL or too small */
+#define BCA_ERR_CAPACITY (-5)         /* the request cannot fit the page table */
+#define BCA_ERR_CUDA (-6)             /* a CUDA runtime/driver call failed */
+#define BCA_ERR_UNSUPPORTED (-7)      /* device is not sm_100-family (tcgen05) */
+#define BCA_ERR_PAGE_SHARED (-8)      /* bca_validate_page_table: page used twice */
+#define BCA_ERR_PAGE_RANGE (-9)       /* bca_validate_page_table: id outside pool */
+/* Device-detected (reported through the workspace status word). */
+#define BCA_ERR_DEVICE_PAGE_OOB (-16) /* a page id outside [0, num_pages) */
+#define BCA_ERR_DEVICE_BAD_LENGTH (-17) /* a length/position outside its range */
+#define BCA_ERR_DEVICE_TIMEOUT (-18)  /* an internal wait gave up (never expected) */
+
+/* Operations, for bca_workspace_size. */
+#define BCA_OP_DECODE 1
+#define BCA_OP_PREFILL 2
+#define BCA_OP_MULTICANVAS 3
+#define BCA_OP_COMMIT 4
+
+/* Shared dimensions of one call.  `version` must be BCA_ABI_VERSION. */
+typedef struct bca_dims {
+  int32_t version;
+  int32_t batch;             /* B: number of sequences */
+  int32_t block_size;        /* D: diffusion block (decode, prefill, commit rows)
+                                or canvas length C (multicanvas) */
+  int32_t num_q_heads;       /* Hq */
+  int32_t num_kv_heads;      /* Hkv */
+  int32_t head_dim;          /* d: 64 or 128 */
+  int32_t page_size;         /* S: tokens per page, multiple of 16 */
+  int32_t num_pages;         /* pages in each pool */
+  int32_t max_pages_per_seq; /* columns of page_table */
+  float softmax_scale;       /* 0 => 1/sqrt(head_dim) */
+} bca_dims;
+
+typedef struct CUstream_st* bca_stream_t; /* == cudaStream_t */
+
+/* Library version (BCA_ABI_VERSION). */
+int bca_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* bca_status_string(int status);
+
+/* Bytes of workspace `op` needs for these dims, or 0 if the dims are invalid.
+ * Decode: a status header, a per-sequence table and fp32 partial results for
+ * splitting long prefixes across CTAs (split-KV); any size >= the value
+ * returned for a smaller batch still works, with less splitting.  Other ops
+ * need only the header. */
+size_t bca_workspace_size(const bca_dims* dims, int op);
+
+/* Zero the workspace header (status word, counters).  Call once after
+ * allocating a workspace; asynchronous on `stream`. */
+int bca_workspace_init(void* workspace, size_t workspace_bytes, bca_stream_t stream);
+
+/* Synchronize `stream`, return the first device-detected error recorded in
+ * the workspace since the last read (BCA_OK if none), and clear it. */
+int bca_read_device_status(void* workspace, bca_stream_t stream);
+
+/* Copy the workspace's tile counters to host memory: counters[0] = key tiles
+ * processed without a mask (fully included), counters[1] = tiles processed
+ * with the elementwise mask (partially included), counters[2] = tiles
+ * skipped (fully excluded, never loaded).  Counters accumulate over calls
+ * until bca_workspace_init.  Synchronizes `stream`. */
+int bca_read_tile_counters(void* workspace, int64_t counters[3], bca_stream_t stream);
+
+/*
+ * bca_decode -- one diffusion-block decode step for a batch.
+ *
+ * "Inference for Interpretable Text-Diffusion Models", "KV Cache", step 2:
+ * the D queries of sequence b's active block (positions P_b .. P_b+D-1,
+ * P_b = prefix_len[b]) attend every key of the completed prefix 0 .. P_b-1,
+ * read through the page table from the pools, and the block's own D keys
+ * (k_blk/v_blk, bidirectionally).  P_b must be a multiple of D ("KV Cache",
+ * step 1: the prefix is whole blocks) and P_b + D <= max_pages_per_seq * S.
+ *
+ * commit = 1 also performs step 3 of the same section in the same call: the
+ * block's K/V bits are copied into positions [P_b, P_b+D) of the pools
+ * (exactly what bca_commit_kv with start_pos = prefix_len does).  The
+ * attention never reads those slots, so the result is the same either way.
+ *
+ * q, out: [B, D, Hq, d] bf16.  k_blk, v_blk: [B, D, Hkv, d] bf16.
+ * k_pool, v_pool: pools (written only when commit = 1).
+ * page_table: int32 [B, max_pages_per_seq].  prefix_len: int32 [B].
+ * A sequence with an invalid prefix length is treated as P_b = 0 and
+ * reported as BCA_ERR_DEVICE_BAD_LENGTH.
+ */
+int bca_decode(const bca_dims* dims, const void* q, const void* k_blk, const void* v_blk,
+               void* k_pool, void* v_pool, const int32_t* page_table,
+               const int32_t* prefix_len, void* out, int commit, void* workspace,
+               size_t workspace_bytes, bca_stream_t stream);
+
+/*
+ * bca_commit_kv -- write finished K/V rows into their pages (a bit copy).
+ *
+ * "Inference for Interpretable Text-Diffusion Models", "KV Cache", step 3,
+ * and "Paged Attention".  For every sequence b and t < num_tokens, row t of
+ * k_blk[b] / v_blk[b] ([B, block_size, Hkv, d]; num_tokens <= block_size) is
+ * copied to logical position start_pos[b] + t.  Slots not targeted keep
+ * their bits.  A target beyond the page table, or a page id outside the pool,
+ * is skipped and reported as a device error.
+ */
+int bca_commit_kv(const bca_dims* dims, const void* k_blk, const void* v_blk, void* k_pool,
+                  void* v_pool, const int32_t* page_table, const int32_t* start_pos,
+                  int32_t num_tokens, void* workspace, size_t workspace_bytes,
+                  bca_stream_t stream);
+
+/*
+ * bca_prefill -- block-causal attention over whole prompts, plus the page
+ * write of their K/V.
+ *
+ * "Inference for Interpretable Text-Diffusion Models", "KV Cache", step 1 and
+ * the prefill BlockMask figure: P0 = 0, every token attends its own block
+ * bidirectionally and earlier blocks causally.  Key tiles of 64 are
+ * classified per query tile of 128 as fully included (no mask), partially
+ * included (elementwise mask) or fully excluded (never loaded)
+ * ("FlexAttention with Aligned Tiles").
+ *
+ * Packed layout: q/out [total_tokens, Hq, d], k/v [total_tokens, Hkv, d];
+ * sequence b occupies rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (int32 [B+1],
+ * device).  max_seqlen: a host-side upper bound of the sequence lengths.
+ * If k_pool is non-NULL, every token t of sequence b is also written to
+ * logical position t of b's pages (the cache fill of step 1).
+ */
+int bca_prefill(const bca_dims* dims, const void* q, const void* k, const void* v,
+                const int32_t* cu_seqlens, int32_t total_tokens, int32_t max_seqlen,
+                void* k_pool, void* v_pool, const int32_t* page_table, void* out,
+                void* workspace, size_t workspace_bytes, bca_stream_t stream);
+
+/*
+ * bca_multicanvas -- multi-canvas shrinking-window attention over an arena.
+ *
+ * "Inference: Fewer, smaller forwards", "Advancement 1", "Advancement 9",
+ * "Advancement 11", "Advancement 13".  dims->block_size is the canvas
+ * length C; P0 = prompt_len.  The queries of sequence b are its live rows:
+ * q_live[b][r] for r < live_count[b], at absolute position live_pos[b][r]
+ * (the active-position index list).  A live row of canvas c sees every key
+ * whose position is below prompt_len + C*(c+1): arena entries (pages of the
+ * pools, the first arena_len[b] slots of b's page list, each with its stored
+ * absolute position kv_pos[page][slot]) and live rows (k_live/v_live at
+ * live_pos).  Every position must be stored exactly once, in the arena or as
+ * a live row; storage order does not matter ("Advancement 10").
+ *
+ * After the attention, rows commit_rows[b][i] (i < commit_count[b], indices
+ * into the live rows) are appended to the arena at slots arena_len[b] + i,
+ * with their positions written to kv_pos, and arena_len[b] is increased by
+ * commit_count[b] ("Advancement 11": promotion appends at the arena end).
+ * commit_rows may be NULL (no promotion).
+ *
+ * q_live/out [B, max_live, Hq, d]; k_live/v_live [B, max_live, Hkv, d];
+ * live_pos int32 [B, max_live] (NULL: row r is at prompt_len + r);
+ * live_count int32 [B] (NULL: max_live); kv_pos int32 [num_pages, S];
+ * arena_len int32 [B]; commit_rows int32 [B, max_commit]; commit_count [B].
+ */
+int bca_multicanvas(const bca_dims* dims, const void* q_live, const void* k_live,
+                    const void* v_live, const int32_t* live_pos, const int32_t* live_count,
+                    int32_t max_live, int32_t prompt_len, int32_t n_canvas, void* k_pool,
+                    void* v_pool, const int32_t* page_table, int32_t* kv_pos,
+                    int32_t* arena_len, const int32_t* commit_rows,
+                    const int32_t* commit_count, int32_t max_commit, void* out,
+                    void* workspace, size_t workspace_bytes, bca_stream_t stream);
+
+/*
+ * bca_validate_page_table -- host-side debug check of a page table (HOST
+ * pointers), for use outside the timed path ("Paged Attention": the page
+ * table is used with stricter error checking).  For each sequence b the first
+ * ceil(used_tokens[b] / page_size) entries must lie in [0, num_pages) and no
+ * page may appear twice among all sequences' used entries.  On failure the
+ * offending (sequence, entry) is written to bad_seq/bad_entry (if non-NULL).
+ */
+int bca_validate_page_table(const bca_dims* dims, const int32_t* page_table_host,
+                            const int32_t* used_tokens_host, int32_t* bad_seq,
+                            int32_t* bad_entry);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BCA_H_ */

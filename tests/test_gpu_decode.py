@@ -1,0 +1,146 @@
+"""GPU parity of bca_decode (and its fused commit) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _gpu_cases import DecodeRun, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _ref(case, seqs=None):
+    return oracle.decode(case.q, case.k_blk, case.v_blk, case.k_prefix, case.v_prefix, seqs=seqs)
+
+
+def test_tiny_decode_and_commit(cuda_lib):
+    """One sequence, 2/1 heads, d=64, D=16 after 48 prefix tokens in a pool of
+    8 shuffled pages; then the block is committed to the 4th logical page."""
+    case = workloads.tiny_decode(seed=0)
+    r = DecodeRun(case)
+    out = r.run(commit=True)
+    assert r.status() == 0
+    assert_close(out, _ref(case), what="tiny")
+    S = case.pool.page_size
+    for name, pool, blk in (("k", r.k_pool, case.k_blk), ("v", r.v_pool, case.v_blk)):
+        src = (case.pool.k_pool if name == "k" else case.pool.v_pool).view(torch.int16).numpy()
+        want = oracle.commit(src, case.pool.page_table, case.prefix_len,
+                             blk.view(torch.int16).numpy(), case.D, S)
+        assert np.array_equal(pool.cpu().view(torch.int16).numpy(), want), name
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_block_decode_batch8(cuda_lib, seed):
+    """Batch 8, 32/8 heads, d=128, D=64, prefix uniform in {512..4096}."""
+    case = workloads.block_decode(seed=seed)
+    r = DecodeRun(case)
+    out = r.run(commit=False)
+    assert r.status() == 0
+    assert_close(out, _ref(case), what=f"block decode seed {seed}")
+
+
+def test_page_permutation_is_bit_identical(cuda_lib):
+    """Scrambling the physical page layout leaves the output bits unchanged."""
+    P = [960, 2048, 64, 3072]
+    a = workloads.make_decode_case(P, D=64, Hq=32, Hkv=8, d=128, seed=7)
+    b = workloads.make_decode_case(P, D=64, Hq=32, Hkv=8, d=128, seed=7, pool_factor=3.0)
+    assert not torch.equal(a.pool.page_table, b.pool.page_table)
+    out_a = DecodeRun(a).run().cpu()
+    out_b = DecodeRun(b).run().cpu()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+@pytest.mark.parametrize("P,D,Hq,Hkv,d", [
+    ([0, 64, 640], 64, 8, 2, 128),        # empty prefix, one prefix tile
+    ([37, 5, 1000], 1, 4, 1, 64),          # block size 1: ordinary causal decode
+    ([17 * 3, 0, 17 * 40], 17, 6, 2, 128),  # ragged block (not a multiple of 16)
+    ([200, 1000], 100, 4, 4, 64),           # G = 1, block of 100 over two M-tiles
+    ([96, 2976], 96, 12, 4, 128),           # G = 3 (rows 126 of 128), 2 row blocks
+    ([4096, 128], 32, 32, 8, 128),         # D = 32: one M-tile per KV head
+])
+def test_generic_shapes(cuda_lib, P, D, Hq, Hkv, d):
+    case = workloads.make_decode_case(P, D=D, Hq=Hq, Hkv=Hkv, d=d, seed=11)
+    r = DecodeRun(case)
+    out = r.run()
+    assert r.status() == 0
+    assert_close(out, _ref(case), what=f"P={P} D={D} {Hq}/{Hkv} d={d}")
+
+
+def test_block_size_one_is_causal_decode(cuda_lib):
+    """D = 1 reduces to single-token causal decode: compare with SDPA on the GPU
+    in fp32 as an independent second reference."""
+    P = [31, 300]
+    case = workloads.make_decode_case(P, D=1, Hq=8, Hkv=2, d=128, seed=3)
+    out = DecodeRun(case).run().cpu().double()
+    for b in range(2):
+        k = torch.cat([case.k_prefix[b], case.k_blk[b]]).double()
+        v = torch.cat([case.v_prefix[b], case.v_blk[b]]).double()
+        q = case.q[b].double()
+        kk = k.repeat_interleave(4, 1).transpose(0, 1)
+        vv = v.repeat_interleave(4, 1).transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(q.transpose(0, 1), kk, vv)
+        err = (out[b] - ref.transpose(0, 1)).abs()
+        assert err.max() < 2e-2 and err.mean() < 2e-3
+
+
+def test_split_kv_matches_unsplit(cuda_lib):
+    """The split-KV path (partials + combine) and a workspace too small to
+    split give the same result within the tolerance."""
+    P = [32768, 128, 9000 // 64 * 64]
+    case = workloads.make_decode_case(P, D=64, Hq=32, Hkv=8, d=128, seed=5)
+    r = DecodeRun(case)
+    ref = _ref(case)
+    a = r.run().clone()
+    assert_close(a, ref, what="split")
+    import block_causal_paged_gb300 as bca
+    small = torch.empty(4096, dtype=torch.uint8, device="cuda")  # header + table only
+    bca.workspace_init(small)
+    b = r.run(ws=small).clone()
+    assert bca.read_device_status(small) == 0
+    assert_close(b, ref, what="unsplit")
+
+
+@pytest.mark.parametrize("D", [64, 32])
+def test_serving_batch64_sampled(cuda_lib, D):
+    """Batch 64, prefix log-uniform in [128, 32768]: the full step on the GPU,
+    the oracle on a sample of sequences (the longest, the shortest, five more)."""
+    case = workloads.serving_decode(seed=0, D=D)
+    r = DecodeRun(case)
+    out = r.run()
+    assert r.status() == 0
+    P = np.array(case.prefix_len)
+    rng = np.random.default_rng(0)
+    seqs = sorted(set([int(P.argmax()), int(P.argmin())] + rng.choice(64, 5, replace=False).tolist()))
+    ref = _ref(case, seqs=seqs)
+    for b in seqs:
+        assert_close(out[b], ref[b], what=f"serving D={D} seq {b} P={P[b]}")
+
+
+def test_device_error_bad_page_is_reported(cuda_lib):
+    import block_causal_paged_gb300 as bca
+    case = workloads.make_decode_case([256, 512], D=64, Hq=8, Hkv=2, d=128, seed=2)
+    r = DecodeRun(case)
+    r.page_table[1, 3] = case.pool.num_pages + 5   # outside the pool
+    r.run()
+    assert r.status() == bca.ERR_DEVICE_PAGE_OOB
+    assert torch.isfinite(r.out.float()).all()
+
+
+def test_device_error_bad_prefix_is_reported(cuda_lib):
+    import block_causal_paged_gb300 as bca
+    case = workloads.make_decode_case([256, 512], D=64, Hq=8, Hkv=2, d=128, seed=2)
+    r = DecodeRun(case)
+    r.prefix_len[0] = 100                           # not a multiple of D
+    r.run()
+    assert r.status() == bca.ERR_DEVICE_BAD_LENGTH
+
+
+def test_tile_counters_decode(cuda_lib):
+    import block_causal_paged_gb300 as bca
+    case = workloads.make_decode_case([640, 64, 0], D=64, Hq=32, Hkv=8, d=128, seed=1)
+    r = DecodeRun(case)
+    r.run()
+    full, partial, skipped = bca.read_tile_counters(r.ws)
+    # per KV head: ceil(P/64) prefix tiles + 1 own-block tile, all fully visible
+    assert (full, partial, skipped) == (8 * ((10 + 1) + (1 + 1) + (0 + 1)), 0, 0)
