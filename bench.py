@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the block-causal decode step on one GB300 (or N, one rank each).
+
+A step is one call of bca_decode with commit on: the attention of a batch of
+64 diffusion blocks (64 masked query tokens each, 32 query / 8 KV heads,
+head_dim 128) over completed prefixes of log-uniform length in [128, 32768]
+held in a paged cache (pages of 16, physical pages in random order, pool of
+twice the need), followed by the commit of the blocks' K/V into the cache.
+Inputs are resident in HBM; the K/V working set (~1.6 GB) is larger than L2,
+so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-step attention µs, TFLOP/s, HBM GB/s and % of roofline at B=64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS)
+
+
+def algorithmic(prefix_len, D, Hq, Hkv, d, S):
+    """Algorithmic work of one decode step: every visible (query, key) pair
+    costs 4d flops per query head; bytes count every input byte once (prefix
+    K/V, Q, the block's K/V, page-table entries, lengths), the output, and
+    the commit writes."""
+    B = len(prefix_len)
+    sumP = sum(prefix_len)
+    flops = 4.0 * d * D * Hq * (sumP + B * D)
+    kv = 2.0 * sumP * Hkv * d * 2
+    q = B * D * Hq * d * 2.0
+    blk = 2.0 * B * D * Hkv * d * 2
+    out = B * D * Hq * d * 2.0
+    pt = 4.0 * sum(math.ceil(P / S) for P in prefix_len) + 4.0 * B
+    attn_bytes = kv + q + blk + out + pt
+    commit_bytes = 2.0 * B * D * Hkv * d * 2  # writes into the pool
+    return {"flops": flops, "attn_bytes": attn_bytes, "step_bytes": attn_bytes + commit_bytes,
+            "sum_prefix": sumP}
+
+
+class ClockSampler:
+    """nvidia-smi samples (timestamped on the host) during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 8]
+        if not rows:
+            rows = [s for (_, s) in self.samples if len(s) >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_on_sequences(seed, prefix_len, D, Hq, Hkv, d, seqs, nthreads):
+    """Run the fp64 oracle on the listed sequences of the workload; returns
+    (seconds, flops) of the oracle calls only."""
+    import oracle
+    import workloads
+    secs, flops = 0.0, 0.0
+    for b in seqs:
+        P = prefix_len[b]
+        kp, vp = workloads.sequence_prefix_kv(seed, b, P, Hkv, d)
+        qb, kb, vb = workloads.sequence_block(seed, b, D, Hq, Hkv, d)
+        t = time.perf_counter()
+        oracle.decode(qb[None], kb[None], vb[None], [kp], [vp], nthreads=nthreads)
+        secs += time.perf_counter() - t
+        flops += 4.0 * d * D * Hq * (P + D)
+    return secs, flops
+
+
+def cpu_baseline(seed, prefix_len, D, Hq, Hkv, d, budget_s=10.0):
+    import numpy as np
+    nthreads = os.cpu_count() or 1
+    order = np.random.default_rng(seed + 1000).permutation(len(prefix_len)).tolist()
+    secs = flops = 0.0
+    used = []
+    for b in order:
+        s, f = oracle_on_sequences(seed, prefix_len, D, Hq, Hkv, d, [b], nthreads)
+        secs += s
+        flops += f
+        used.append(b)
+        if secs >= budget_s:
+            break
+    keys = sum(prefix_len[b] + D for b in used)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(used)} of {len(prefix_len)} sequences of the same step "
+                      f"({keys} of {sum(prefix_len) + D * len(prefix_len)} keys), fp64, "
+                      f"{secs:.1f} s of oracle time"}
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle, as it stands, on host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import workloads
+    D, Hq, Hkv, d = args.D, 32, 8, 128
+    prefix_len = workloads.prefix_loguniform_blocks(64, 128, 32768, 64, args.seed)
+    nthreads = os.cpu_count() or 1
+    # each step: the oracle on one sequence of the workload, the one whose
+    # estimated cost is closest to the per-step budget that keeps the whole
+    # --steps/--warmup run within a few minutes
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    est_rate = 1.5e10  # fp64 flop/s of the oracle on a many-core host (estimate)
+    b_pick = min(range(64), key=lambda x: abs(4.0 * d * D * Hq * (prefix_len[x] + D) / est_rate
+                                              - budget))
+    step_seqs = [b_pick] * (args.steps + args.warmup)
+    secs = flops = 0.0
+    for i, b in enumerate(step_seqs):
+        s, f = oracle_on_sequences(args.seed, prefix_len, D, Hq, Hkv, d, [b], nthreads)
+        if i >= args.warmup:
+            secs += s
+            flops += f
+    value = flops / secs / 1e12 if secs > 0 else 0.0
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args, prefix_len),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads,
+                             "kind": "oracle",
+                             "sample": f"sequence {b_pick} of the batch (prefix "
+                                       f"{prefix_len[b_pick]}) per step, fp64 oracle with an "
+                                       "explicit dense mask"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attention.cu", "ptx_sm103.cuh", "bca_internal.h"):
+        with open(os.path.join(ROOT, "block_causal_paged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def committed_traffic(batch, D):
+    """DRAM bytes per attention launch from the committed ncu summary, scaled
+    to this workload; None if the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "attention_decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None, "no committed capture"
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None, "kernel changed since the capture"
+    if rec.get("batch") == batch and rec.get("D") == D:
+        return float(rec["dram_bytes_per_launch"]), rec.get("command", "")
+    return None, "capture is for another workload"
+
+
+def workload_config(args, prefix_len):
+    return {"workload": f"serving decode step: batch {args.batch} x 1 block of D={args.D} query tokens, "
+                        f"32 q / 8 kv heads, head_dim 128, prefix log-uniform in [128, 32768] "
+                        f"rounded to 64 (sum {sum(prefix_len)} tokens, seed {args.seed}), "
+                        f"page size 16, pool 2x need in random physical order, KV commit on",
+            "batch_per_gpu": args.batch, "global_batch": args.batch * args.gpus, "block_size": args.D,
+            "seq_len_max": 32768, "heads": "32/8", "head_dim": 128, "page_size": 16,
+            "softmax_scale": "1/sqrt(128)", "inputs": "N(0,1) bf16",
+            "l2": "inputs larger than L2 (KV working set ~1.6 GB), no flush",
+            "parallelism": f"{args.gpus} independent replicas, each with its own batch "
+                           "(no collective on the data path)"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def time_steps(torch, fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import block_causal_paged_gb300 as bca
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bca.load()
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def build_case(D):
+        # each rank runs its own batch (weak scaling): seed offset by rank
+        case = workloads.serving_decode(seed=args.seed + rank, D=D, B=args.batch,
+                                        keep_logical=False)
+        S = case.pool.page_size
+        dd = bca.dims(case.B, D, case.Hq, case.Hkv, case.d, S, case.pool.num_pages,
+                      case.pool.max_pages_per_seq)
+        t = dict(q=case.q.to(dev), kb=case.k_blk.to(dev), vb=case.v_blk.to(dev),
+                 kp=case.pool.k_pool.to(dev), vp=case.pool.v_pool.to(dev),
+                 pt=case.pool.page_table.to(dev),
+                 pl=torch.tensor(case.prefix_len, dtype=torch.int32, device=dev))
+        t["out"] = torch.empty_like(t["q"])
+        t["ws"] = bca.new_workspace(dd, bca.OP_DECODE, device=dev)
+        return case, dd, t
+
+    def step_fn(dd, t):
+        return lambda: bca.bca_decode(dd, t["q"], t["kb"], t["vb"], t["kp"], t["vp"], t["pt"],
+                                      t["pl"], t["out"], True, t["ws"])
+
+    def measure(D, steps, warmup, with_clocks):
+        case, dd, t = build_case(D)
+        step = step_fn(dd, t)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        st = bca.read_device_status(t["ws"])
+        if st != 0:
+            raise RuntimeError(f"device status after warm-up: {bca.status_string(st)}")
+        sampler = ClockSampler(local) if with_clocks else None
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        barrier()
+        t0 = time.time()
+        ms = time_steps(torch, step, steps, stream)
+        t1 = time.time()
+        barrier()
+        clocks = None
+        if sampler:
+            time.sleep(0.15)
+            sampler.stop()
+            clocks = sampler.summary(t0, t1)
+        # per-kernel device time, CUDA events on the launch stream (separate pass)
+        bca.profile_start(steps * 4 + 16)
+        for _ in range(steps):
+            step()
+        torch.cuda.synchronize()
+        prof = bca.profile_stop()
+        alg = algorithmic(case.prefix_len, D, case.Hq, case.Hkv, case.d, case.pool.page_size)
+        return case, dd, t, ms / steps, clocks, prof, alg
+
+    case, dd, t, ms_step, clocks, prof, alg = measure(args.D, args.steps, args.warmup, True)
+    ms_all = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_all, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_all.item())
+    flops_total = alg["flops"] * world  # every rank runs the same-shaped workload
+    value = flops_total / (ms_max * 1e-3) / 1e12
+
+    traffic, traffic_src = committed_traffic(args.batch, args.D)
+    if args.traffic is not None:
+        traffic, traffic_src = args.traffic, "--traffic"
+    attn_n, attn_ms = prof["attention"]
+    attn_avg_ms = attn_ms / max(1, attn_n)
+    achieved_gbs = alg["attn_bytes"] / (attn_avg_ms * 1e-3) / 1e9
+    achieved_tflops = alg["flops"] / (attn_avg_ms * 1e-3) / 1e12
+    t_mem = alg["attn_bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_flop = alg["flops"] / (pk["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_mem >= t_flop else "tensor"
+    roofline = {
+        "kernel": "attention (bca_decode main kernel)",
+        "bound": bound,
+        "achieved": achieved_gbs if bound == "hbm" else achieved_tflops,
+        "peak": pk["hbm_gbs"] if bound == "hbm" else pk["bf16_tflops"],
+        "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+        "frac": (achieved_gbs / pk["hbm_gbs"]) if bound == "hbm" else (achieved_tflops / pk["bf16_tflops"]),
+        "traffic": traffic,
+        "traffic_source": traffic_src,
+        "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs / bf16_tflops burst)"
+                       if pk["source"] == "measured" else "fallback",
+        "kernel_us": attn_avg_ms * 1e3,
+        "algorithmic_bytes": alg["attn_bytes"],
+        "algorithmic_flops": alg["flops"],
+        "tensor_frac": achieved_tflops / pk["bf16_tflops"],
+        "step_roofline_frac": max(alg["step_bytes"] / (pk["hbm_gbs"] * 1e9),
+                                  alg["flops"] / (pk["bf16_tflops"] * 1e12)) / (ms_max * 1e-3),
+    }
+    launches_per_step = sum(n for n, _ in prof.values()) / max(1, args.steps)
+
+    # end to end through the public API with pinned host buffers
+    h = {k: t[k].cpu().pin_memory() for k in ("q", "kb", "vb", "pt", "pl")}
+    h_out = torch.empty(t["out"].shape, dtype=t["out"].dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in h.values())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for k in h:
+            t[k].copy_(h[k], non_blocking=True)
+        bca.bca_decode(dd, t["q"], t["kb"], t["vb"], t["kp"], t["vp"], t["pt"], t["pl"],
+                       t["out"], True, t["ws"])
+        h_out.copy_(t["out"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    e2e_steps = max(10, args.steps // 4)
+    barrier()
+    e2e_ms = time_steps(torch, e2e_step, e2e_steps, stream) / e2e_steps
+    e_all = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e_all, op=dist.ReduceOp.MAX)
+    e2e_value = flops_total / (float(e_all.item()) * 1e-3) / 1e12
+    st = bca.read_device_status(t["ws"])
+    del t, case
+
+    sweep = []
+    if not args.no_sweep:
+        for D2 in (32, 64):
+            if D2 == args.D:
+                sweep.append({"D": D2, "us_per_step": ms_max * 1e3, "tflops": value / world,
+                              "attn_us": attn_avg_ms * 1e3, "attn_hbm_frac": roofline["frac"]})
+                continue
+            c2, _, t2, ms2, _, prof2, alg2 = measure(D2, max(20, args.steps // 2),
+                                                     max(3, args.warmup), False)
+            n2, tot2 = prof2["attention"]
+            a2 = tot2 / max(1, n2)
+            sweep.append({"D": D2, "us_per_step": ms2 * 1e3,
+                          "tflops": alg2["flops"] / (ms2 * 1e-3) / 1e12, "attn_us": a2 * 1e3,
+                          "attn_hbm_frac": alg2["attn_bytes"] / (a2 * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "sum_prefix": alg2["sum_prefix"]})
+            del t2, c2
+
+    if rank == 0:
+        prefix_len = workloads.prefix_loguniform_blocks(args.batch, 128, 32768, 64, args.seed)
+        cpu = None if args.no_cpu_baseline else cpu_baseline(args.seed, prefix_len, args.D, 32, 8,
+                                                             128, args.cpu_seconds)
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "us_per_step": ms_max * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(args, prefix_len),
+                "hbm_gbs": alg["step_bytes"] / (ms_max * 1e-3) / 1e9,
+                "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": float(e_all.item())},
+                "gpu_launches": int(round(launches_per_step * args.steps)),
+                "launches_per_step": launches_per_step,
+                "kernel_ms": {k: (v[1] / v[0] if v[0] else None) for k, v in prof.items()},
+                "clocks": clocks, "device_status": st, "sweep": sweep}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--D", type=int, default=64, choices=[32, 64])
+    ap.add_argument("--batch", type=int, default=64,
+                    help="sequences per GPU (64 is the benchmarked configuration; smaller "
+                         "batches are for profiler captures)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per attention launch from an ncu capture (reported as is)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -45,6 +45,13 @@ class Dims(ctypes.Structure):
                 ("softmax_scale", _f)]
 
 
+class KernelTimes(ctypes.Structure):
+    """struct bca_kernel_times."""
+    _fields_ = [("launches", _i32 * 4), ("total_ms", ctypes.c_double * 4)]
+
+
+KERNEL_NAMES = ("attention", "combine", "commit", "promote")
+
 _DP = ctypes.POINTER(Dims)
 SIGNATURES = {
     "bca_version": ([], ctypes.c_int),
@@ -62,6 +69,8 @@ SIGNATURES = {
                          _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp], ctypes.c_int),
     "bca_validate_page_table": ([_DP, _vp, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)],
                                 ctypes.c_int),
+    "bca_profile_start": ([_i32], ctypes.c_int),
+    "bca_profile_stop": ([ctypes.POINTER(KernelTimes)], ctypes.c_int),
 }
 
 _lib = None
@@ -198,6 +207,17 @@ def bca_validate_page_table(d: Dims, page_table_host, used_tokens_host) -> tuple
     rc = load().bca_validate_page_table(ctypes.byref(d), _ptr(page_table_host),
                                         _ptr(used_tokens_host), ctypes.byref(bs), ctypes.byref(be))
     return int(rc), int(bs.value), int(be.value)
+
+
+def profile_start(max_launches: int = 4096) -> None:
+    _check(load().bca_profile_start(int(max_launches)), "bca_profile_start")
+
+
+def profile_stop() -> dict:
+    """{kernel name: (launches, total device ms)} since profile_start."""
+    t = KernelTimes()
+    _check(load().bca_profile_stop(ctypes.byref(t)), "bca_profile_stop")
+    return {n: (int(t.launches[i]), float(t.total_ms[i])) for i, n in enumerate(KERNEL_NAMES)}
 
 
 def default_scale(head_dim: int) -> float:

@@ -168,6 +168,43 @@ AttnParams base_params(const bca_dims* d) {
   return p;
 }
 
+// ---------------------------------------------------------------------------
+// optional kernel timing (bca_profile_start / bca_profile_stop)
+// ---------------------------------------------------------------------------
+struct Profile {
+  std::mutex mu;
+  bool active = false;
+  std::vector<cudaEvent_t> ev;     // 2 per slot
+  std::vector<int> kind;           // per used slot
+  int used = 0;
+};
+Profile g_prof;
+
+// Returns a slot index (or -1) and records its start event on `s`.
+int prof_begin(int k, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.active || g_prof.used * 2 >= (int)g_prof.ev.size()) return -1;
+  const int i = g_prof.used++;
+  g_prof.kind[i] = k;
+  cudaEventRecord(g_prof.ev[2 * i], s);
+  return i;
+}
+
+void prof_end(int i, cudaStream_t s) {
+  if (i < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  cudaEventRecord(g_prof.ev[2 * i + 1], s);
+}
+
+// Launch helper: times the launch when a profile is active.
+template <typename F>
+cudaError_t timed(int k, cudaStream_t s, F&& launch) {
+  const int i = prof_begin(k, s);
+  const cudaError_t e = launch();
+  prof_end(i, s);
+  return e;
+}
+
 }  // namespace
 
 DecodeWsLayout decode_ws_layout(int B, int head_dim, size_t ws_bytes) {
@@ -293,7 +330,9 @@ int bca_commit_kv(const bca_dims* d, const void* k_blk, const void* v_blk, void*
   c.num_pages = d->num_pages;
   c.max_pages = d->max_pages_per_seq;
   c.hdr = (WsHeader*)ws;
-  return launch_commit(c, (cudaStream_t)stream) == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+  return timed(BCA_KERNEL_COMMIT, (cudaStream_t)stream, [&] { return launch_commit(c, (cudaStream_t)stream); }) == cudaSuccess
+             ? BCA_OK
+             : BCA_ERR_CUDA;
 }
 
 int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* v_blk,
@@ -352,9 +391,11 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
       (long long)d->batch * d->num_kv_heads * p.n_rb * ceil_div_i(max_tiles, kChMin);
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_attention(p, maps, HD, grid, s) != cudaSuccess) return BCA_ERR_CUDA;
+  if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
+    return BCA_ERR_CUDA;
   if (max_tiles > kChMin) {
-    if (launch_decode_combine(p, HD, s) != cudaSuccess) return BCA_ERR_CUDA;
+    if (timed(BCA_KERNEL_COMBINE, s, [&] { return launch_decode_combine(p, HD, s); }) != cudaSuccess)
+      return BCA_ERR_CUDA;
   }
   if (commit) {
     CommitParams c;
@@ -375,7 +416,7 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
     c.num_pages = d->num_pages;
     c.max_pages = d->max_pages_per_seq;
     c.hdr = p.hdr;
-    if (launch_commit(c, s) != cudaSuccess) return BCA_ERR_CUDA;
+    if (timed(BCA_KERNEL_COMMIT, s, [&] { return launch_commit(c, s); }) != cudaSuccess) return BCA_ERR_CUDA;
   }
   return BCA_OK;
 }
@@ -428,7 +469,8 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
                               d->num_kv_heads * p.n_hp;
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_attention(p, maps, HD, grid, s) != cudaSuccess) return BCA_ERR_CUDA;
+  if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
+    return BCA_ERR_CUDA;
   if (k_pool) {
     CommitParams c;
     std::memset(&c, 0, sizeof(c));
@@ -446,7 +488,7 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
     c.num_pages = d->num_pages;
     c.max_pages = d->max_pages_per_seq;
     c.hdr = p.hdr;
-    if (launch_commit(c, s) != cudaSuccess) return BCA_ERR_CUDA;
+    if (timed(BCA_KERNEL_COMMIT, s, [&] { return launch_commit(c, s); }) != cudaSuccess) return BCA_ERR_CUDA;
   }
   return BCA_OK;
 }
@@ -512,7 +554,8 @@ int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
       (long long)d->batch * d->num_kv_heads * ceil_div_i(max_live, 2 * p.tpm);
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_attention(p, maps, HD, grid, s) != cudaSuccess) return BCA_ERR_CUDA;
+  if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
+    return BCA_ERR_CUDA;
   if (commit_rows && max_commit > 0) {
     PromoteParams c;
     std::memset(&c, 0, sizeof(c));
@@ -537,7 +580,7 @@ int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
     c.max_commit = max_commit;
     c.prompt_len = prompt_len;
     c.hdr = p.hdr;
-    if (launch_promote(c, s) != cudaSuccess) return BCA_ERR_CUDA;
+    if (timed(BCA_KERNEL_PROMOTE, s, [&] { return launch_promote(c, s); }) != cudaSuccess) return BCA_ERR_CUDA;
   }
   return BCA_OK;
 }
@@ -571,6 +614,53 @@ int bca_validate_page_table(const bca_dims* d, const int32_t* pt, const int32_t*
     }
   }
   return BCA_OK;
+}
+
+int bca_profile_start(int32_t max_launches) {
+  if (max_launches < 1 || max_launches > (1 << 20)) return BCA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.active) return BCA_ERR_INVALID_ARG;
+  g_prof.ev.assign((size_t)max_launches * 2, nullptr);
+  for (auto& e : g_prof.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      for (auto& x : g_prof.ev)
+        if (x) cudaEventDestroy(x);
+      g_prof.ev.clear();
+      return BCA_ERR_CUDA;
+    }
+  }
+  g_prof.kind.assign((size_t)max_launches, -1);
+  g_prof.used = 0;
+  g_prof.active = true;
+  return BCA_OK;
+}
+
+int bca_profile_stop(bca_kernel_times* out) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.active) return BCA_ERR_INVALID_ARG;
+  bca_kernel_times t;
+  std::memset(&t, 0, sizeof(t));
+  int rc = BCA_OK;
+  for (int i = 0; i < g_prof.used; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) {
+      rc = BCA_ERR_CUDA;
+      continue;
+    }
+    const int k = g_prof.kind[i];
+    if (k >= 0 && k < BCA_KERNEL_KINDS) {
+      t.launches[k] += 1;
+      t.total_ms[k] += ms;
+    }
+  }
+  for (auto& e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  g_prof.kind.clear();
+  g_prof.used = 0;
+  g_prof.active = false;
+  if (out) *out = t;
+  return rc;
 }
 
 }  // extern "C"

@@ -675,7 +675,8 @@ __device__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap*
       for (int m = 0; m < n_m; ++m) {
         if (!wait_bar_warp(c, p, &c.bar.q_empty[m], (qn[m] & 1) ^ 1)) { ok = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&c.bar.q_full[m], C::kQBytes);
+          // the Q box holds hpr x tpm rows (126 for G = 3), 128 bytes per row per half
+          mbar_arrive_expect_tx(&c.bar.q_full[m], (uint32_t)(C::kHalves * p.hpr * p.tpm * 128));
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h)
             tma_load_3d(q_base + m * C::kQBytes + h * 16384, tm_q, &c.bar.q_full[m], h * 64,

@@ -236,6 +236,30 @@ int bca_validate_page_table(const bca_dims* dims, const int32_t* page_table_host
                             const int32_t* used_tokens_host, int32_t* bad_seq,
                             int32_t* bad_entry);
 
+/*
+ * Kernel timing for benchmarks (not on any computation path).  While a
+ * profile is active, every entry point records a CUDA event pair around each
+ * kernel it launches, on the call's own stream; bca_profile_stop synchronizes
+ * those events and returns, per kernel kind, the number of launches and their
+ * summed device time.  Host-side state, one profile per process; the event
+ * pairs are created by bca_profile_start (max_launches of them) and destroyed
+ * by bca_profile_stop.  Launches beyond max_launches are not timed.  Do not
+ * use while a stream is being captured into a CUDA graph.
+ */
+#define BCA_KERNEL_ATTENTION 0 /* the block-causal attention kernel */
+#define BCA_KERNEL_COMBINE 1   /* split-KV combine (decode) */
+#define BCA_KERNEL_COMMIT 2    /* KV commit / prefill page write */
+#define BCA_KERNEL_PROMOTE 3   /* multicanvas arena promotion */
+#define BCA_KERNEL_KINDS 4
+
+typedef struct bca_kernel_times {
+  int32_t launches[BCA_KERNEL_KINDS];
+  double total_ms[BCA_KERNEL_KINDS];
+} bca_kernel_times;
+
+int bca_profile_start(int32_t max_launches);
+int bca_profile_stop(bca_kernel_times* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -128,6 +128,15 @@ def write_logical_into_pool(pool: PagedPool, b: int, k_log: torch.Tensor, v_log:
     """
     S = pool.page_size
     n = k_log.shape[0]
+    if n == 0:
+        return
+    if start % S == 0 and n % S == 0:
+        # whole pages: one indexed assignment
+        pages = pool.page_table[b, start // S:(start + n) // S].long()
+        shape = (n // S, S) + tuple(k_log.shape[1:])
+        pool.k_pool[pages] = k_log.reshape(shape).transpose(1, 2)
+        pool.v_pool[pages] = v_log.reshape(shape).transpose(1, 2)
+        return
     for p0 in range(start - start % S, start + n, S):
         page = int(pool.page_table[b, p0 // S])
         lo, hi = max(p0, start), min(p0 + S, start + n)
