@@ -31,7 +31,7 @@ ERR_DEVICE_PAGE_OOB = -16
 ERR_DEVICE_BAD_LENGTH = -17
 ERR_DEVICE_TIMEOUT = -18
 
-OP_DECODE, OP_PREFILL, OP_MULTICANVAS, OP_COMMIT = 1, 2, 3, 4
+OP_DECODE, OP_PREFILL, OP_MULTICANVAS, OP_COMMIT, OP_DECODE_MIN = 1, 2, 3, 4, 5
 
 # Every C entry point of include/bca.h, with its ctypes signature.
 _vp, _i32, _i64, _sz, _f = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -47,10 +47,10 @@ class Dims(ctypes.Structure):
 
 class KernelTimes(ctypes.Structure):
     """struct bca_kernel_times."""
-    _fields_ = [("launches", _i32 * 4), ("total_ms", ctypes.c_double * 4)]
+    _fields_ = [("launches", _i32 * 5), ("total_ms", ctypes.c_double * 5)]
 
 
-KERNEL_NAMES = ("attention", "combine", "commit", "promote")
+KERNEL_NAMES = ("attention", "combine", "commit", "promote", "plan")
 
 _DP = ctypes.POINTER(Dims)
 SIGNATURES = {

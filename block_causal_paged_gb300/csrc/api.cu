@@ -207,21 +207,29 @@ cudaError_t timed(int k, cudaStream_t s, F&& launch) {
 
 }  // namespace
 
-DecodeWsLayout decode_ws_layout(int B, int head_dim, size_t ws_bytes) {
+DecodeWsLayout decode_ws_layout(int B, int Hkv, int n_rb, int head_dim, int n_sms,
+                                size_t ws_bytes) {
   DecodeWsLayout l;
   l.split_base_off = kWsHeaderBytes;
-  l.ml_off = l.split_base_off + round_up((size_t)(B > 0 ? B : 1) * 4, 256);
+  l.items_off = l.split_base_off + round_up((size_t)(B > 0 ? B : 1) * 4, 256);
+  l.items_cap = n_sms * kWaves + B * Hkv * n_rb;
+  l.ml_off = l.items_off + round_up((size_t)l.items_cap * 32, 256);
   l.bytes_per_slot = 256 * 2 * 4 + (size_t)256 * head_dim * 4;
   l.cap = 0;
-  if (ws_bytes > l.ml_off + 256) l.cap = (int)std::min<size_t>((ws_bytes - l.ml_off - 256) / l.bytes_per_slot, 1 << 30);
+  if (ws_bytes > l.ml_off + 256)
+    l.cap = (int)std::min<size_t>((ws_bytes - l.ml_off - 256) / l.bytes_per_slot, 1 << 30);
   l.o_off = l.ml_off + round_up((size_t)l.cap * 256 * 2 * 4, 256);
   return l;
 }
 
+size_t decode_ws_minimum(int B, int Hkv, int n_rb, int head_dim, int n_sms) {
+  return decode_ws_layout(B, Hkv, n_rb, head_dim, n_sms, 0).ml_off;
+}
+
 size_t decode_ws_recommended(int B, int Hkv, int n_rb, int head_dim, int n_sms) {
-  DecodeWsLayout l = decode_ws_layout(B, head_dim, 0);
-  const size_t cap = (size_t)n_sms * kWaves + (size_t)B * Hkv * n_rb;
-  return l.ml_off + cap * l.bytes_per_slot + 512;
+  DecodeWsLayout l = decode_ws_layout(B, Hkv, n_rb, head_dim, n_sms, 0);
+  // split slots never exceed the work items
+  return l.ml_off + (size_t)l.items_cap * l.bytes_per_slot + 512;
 }
 
 }  // namespace bca
@@ -253,14 +261,16 @@ const char* bca_status_string(int s) {
 
 size_t bca_workspace_size(const bca_dims* d, int op) {
   if (validate_dims(d) != BCA_OK) return 0;
-  if (op == BCA_OP_DECODE) {
+  if (op == BCA_OP_DECODE || op == BCA_OP_DECODE_MIN) {
     DeviceInfo di;
     int sms = 160;
     if (device_info(&di) == BCA_OK) sms = di.sms;
     const int G = d->num_q_heads / d->num_kv_heads;
     const int tpm = 128 / G;
     const int n_rb = ceil_div_i(d->block_size, 2 * tpm);
-    return decode_ws_recommended(d->batch, d->num_kv_heads, n_rb, d->head_dim, sms);
+    return op == BCA_OP_DECODE
+               ? decode_ws_recommended(d->batch, d->num_kv_heads, n_rb, d->head_dim, sms)
+               : decode_ws_minimum(d->batch, d->num_kv_heads, n_rb, d->head_dim, sms);
   }
   if (op == BCA_OP_PREFILL || op == BCA_OP_MULTICANVAS || op == BCA_OP_COMMIT)
     return kWsHeaderBytes;
@@ -351,10 +361,14 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
   if (d->block_size > cap_tokens) return BCA_ERR_CAPACITY;
   const long long q_tokens = (long long)d->batch * d->block_size;
   if (q_tokens * d->num_q_heads >= (1ll << 31)) return BCA_ERR_INVALID_ARG;
-  const DecodeWsLayout lay = decode_ws_layout(d->batch, d->head_dim, ws_bytes);
-  if (ws_bytes < lay.ml_off) return BCA_ERR_WORKSPACE;
+  if (ws_bytes < kWsHeaderBytes + round_up((size_t)d->batch * 4, 256)) return BCA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((rc = device_info(&di))) return rc;
+  const int G0 = d->num_q_heads / d->num_kv_heads;
+  const int n_rb0 = ceil_div_i(d->block_size, 2 * (128 / G0));
+  const DecodeWsLayout lay =
+      decode_ws_layout(d->batch, d->num_kv_heads, n_rb0, d->head_dim, di.sms, ws_bytes);
+  if (ws_bytes < lay.ml_off) return BCA_ERR_WORKSPACE;
 
   AttnParams p = base_params(d);
   p.mode = kModeDecode;
@@ -372,6 +386,8 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
   p.out = (uint16_t*)out;
   p.hdr = (WsHeader*)ws;
   p.split_base = (int32_t*)((char*)ws + lay.split_base_off);
+  p.items = (int4*)((char*)ws + lay.items_off);
+  p.items_cap = lay.items_cap;
   p.part_ml = (float*)((char*)ws + lay.ml_off);
   p.part_o = (float*)((char*)ws + lay.o_off);
   p.split_cap = lay.cap;
@@ -391,6 +407,8 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
       (long long)d->batch * d->num_kv_heads * p.n_rb * ceil_div_i(max_tiles, kChMin);
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
   cudaStream_t s = (cudaStream_t)stream;
+  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
+    return BCA_ERR_CUDA;
   if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;
   if (max_tiles > kChMin) {
@@ -448,6 +466,7 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
   p.tpm = 128;
   p.n_hp = (p.G + 1) / 2;
   p.n_rb = 1;
+  p.n_qt_max = ceil_div_i(max_seqlen, 128);
   p.page_table = page_table;
   p.lens = cu_seqlens;
   p.k_dense = (const uint16_t*)k;
@@ -469,6 +488,8 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
                               d->num_kv_heads * p.n_hp;
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
   cudaStream_t s = (cudaStream_t)stream;
+  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
+    return BCA_ERR_CUDA;
   if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;
   if (k_pool) {
@@ -525,6 +546,7 @@ int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
   p.tpm = 128 / p.G;
   p.n_hp = 1;
   p.n_rb = 1;
+  p.n_rb_max = ceil_div_i(max_live, 2 * p.tpm);
   p.page_table = page_table;
   p.lens = live_count;
   p.live_pos = live_pos;
@@ -554,6 +576,8 @@ int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
       (long long)d->batch * d->num_kv_heads * ceil_div_i(max_live, 2 * p.tpm);
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
   cudaStream_t s = (cudaStream_t)stream;
+  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
+    return BCA_ERR_CUDA;
   if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;
   if (commit_rows && max_commit > 0) {

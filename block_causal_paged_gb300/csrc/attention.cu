@@ -1,6 +1,7 @@
 // Block-causal attention over a paged KV cache, sm_103a (tcgen05 + TMA).
 //
-// One persistent CTA per SM walks a static list of work items.  An item is a
+// One persistent CTA per SM takes work items from a shared counter (a small
+// plan kernel orders them longest first and resets the counter).  An item is a
 // block of up to 256 query rows (two M-tiles of 128 rows) that share one KV
 // head, plus the sequence of 64-key tiles those rows attend.  Rows are
 // (token, head) pairs: for decode and multicanvas the G query heads of one KV
@@ -22,8 +23,9 @@
 //   warp 0      loader   : TMA loads of Q and of K/V page boxes into a ring of
 //                          shared-memory stages (ragged 16-key chunks are
 //                          copied by the warp's lanes with zero fill)
-//   warp 1      MMA      : one thread issues tcgen05.mma: S = Q K^T into TMEM,
-//                          O += P V into TMEM (the two M-tiles ping-pong)
+//   warp 1      MMA      : one thread issues tcgen05.mma: S = Q K^T into one of
+//                          two TMEM buffers per M-tile (S of tile j+2 is issued
+//                          while the softmax works on tile j), O += P V into TMEM
 //   warp 2      TMEM allocation / release
 //   warps 4-7   softmax for M-tile 0, warps 8-11 for M-tile 1: read S rows
 //               from TMEM, mask, online softmax (lazy rescale of O), write P
@@ -73,14 +75,15 @@ struct Cfg {
   static constexpr int kOffP = kOffQ + 2 * kQBytes;
   static constexpr int kOffKV = kOffP + 2 * kPBytes;
   static constexpr int kOffRec = kOffKV + kStages * kSlotBytes;
-  static constexpr int kNumBars = 2 * kNumRec + 2 * kStages + 12 + 1;
+  static constexpr int kNumBars = 2 * kNumRec + 2 * kStages + 20 + 1;
   static constexpr int kOffBar = kOffRec + kNumRec * (int)sizeof(Rec);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kSmemAlloc = kBytes + 1024;  // base is aligned up to 1024 in the kernel
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kColS = 0;     // S of M-tile m at column 64*m
-  static constexpr int kColO = 128;   // O of M-tile m at column 128 + HD*m
+  // TMEM columns: S of M-tile m, buffer b at 64*(2m+b); O of M-tile m at 256 + HD*m
+  static constexpr int kColS = 0;
+  static constexpr int kColO = 256;
   static_assert(kColO + 2 * HD <= (int)kTmemCols, "TMEM plan");
   static_assert(kSmemAlloc <= 232448, "shared memory plan");
 };
@@ -90,12 +93,14 @@ struct Bars {
   uint64_t* rec_empty;
   uint64_t* kv_full;
   uint64_t* kv_empty;
-  uint64_t* q_full;
-  uint64_t* q_empty;
-  uint64_t* s_full;
-  uint64_t* p_full;
-  uint64_t* o_full;
-  uint64_t* o_empty;
+  uint64_t* q_full;    // [2]
+  uint64_t* q_empty;   // [2]
+  uint64_t* s_full;    // [2 M-tiles][2 buffers]
+  uint64_t* s_free;    // [2][2]
+  uint64_t* p_full;    // [2]
+  uint64_t* pv_done;   // [2]
+  uint64_t* o_full;    // [2]
+  uint64_t* o_empty;   // [2]
   uint64_t* drain;
 };
 
@@ -295,90 +300,22 @@ struct Planner {
   }
 
   // --------------------------------------------------------------------------
-  __device__ int decode_prefix(int b, int* bad) const {
-    const int P = __ldg(p.lens + b);
-    const long long cap = (long long)p.max_pages * p.S;
-    if (P < 0 || P % p.Dblk != 0 || (long long)P + p.Dblk > cap) {
-      *bad = 1;
-      return 0;
-    }
-    return P;
-  }
-  __device__ int decode_tiles(int P) const {
-    return ceil_div(P, kTileKeys) + ceil_div(p.Dblk, kTileKeys);
+  // Next work item from the shared counter (the plan kernel reset it).
+  __device__ int grab() {
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(&p.hdr->work_next, 1);
+    return __shfl_sync(0xffffffffu, idx, 0);
   }
 
+  // Decode items come from the plan kernel's list, longest sequences first:
+  // {b, g, rb, split slot} {first tile, end tile, prefix length, -}.
   __device__ void run_decode() {
-    const int B = p.B, D = p.Dblk;
-    const int per_seq = p.Hkv * p.n_rb;
-    int bad = 0;
-    long long tot = 0;
-    for (int b0 = 0; b0 < B; b0 += 32) {
-      const int b = b0 + lane;
-      if (b < B) tot += decode_tiles(decode_prefix(b, &bad));
-    }
-    tot = warp_sum_ll(tot) * per_seq;
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, kErrBadLength);
-    const long long target = (long long)gridDim.x * max(1, p.waves);
-    long long ch = (tot + target - 1) / target;
-    int CH = (int)(ch > (long long)max(1, p.ch_min) ? ch : (long long)max(1, p.ch_min));
-    // respect the split workspace capacity
-    for (int guard = 0; guard < 40; ++guard) {
-      long long ns = 0;
-      for (int b0 = 0; b0 < B; b0 += 32) {
-        const int b = b0 + lane;
-        if (b < B) {
-          int dummy = 0;
-          const int nch = ceil_div(decode_tiles(decode_prefix(b, &dummy)), CH);
-          if (nch > 1) ns += nch;
-        }
-      }
-      ns = warp_sum_ll(ns) * per_seq;
-      if (ns <= p.split_cap) break;
-      CH = CH > (1 << 29) ? CH : CH * 2;
-    }
-    if (blockIdx.x == 0 && lane == 0) p.hdr->chunk_tiles = CH;
-
-    long long next = blockIdx.x, item_off = 0, split_off = 0;
-    for (int b0 = 0; b0 < B && ok; b0 += 32) {
-      const int b = b0 + lane;
-      int P = 0, nt = 0, nch = 0;
-      long long items = 0, splits = 0;
-      if (b < B) {
-        int dummy = 0;
-        P = decode_prefix(b, &dummy);
-        nt = decode_tiles(P);
-        nch = ceil_div(nt, CH);
-        items = (long long)nch * per_seq;
-        splits = nch > 1 ? items : 0;
-      }
-      const long long exi = warp_excl_scan_ll(items, lane);
-      const long long exs = warp_excl_scan_ll(splits, lane);
-      const long long win_items = warp_sum_ll(items);
-      const long long win_splits = warp_sum_ll(splits);
-      if (blockIdx.x == 0 && b < B) p.split_base[b] = (int)(split_off + exs);
-      while (ok && next < item_off + win_items) {
-        const long long local = next - item_off;
-        const unsigned own = __ballot_sync(0xffffffffu, b < B && local >= exi && local < exi + items);
-        const int src = __ffs(own) - 1;
-        const int bo = b0 + src;
-        const int Po = __shfl_sync(0xffffffffu, P, src);
-        const int nto = __shfl_sync(0xffffffffu, nt, src);
-        const int ncho = __shfl_sync(0xffffffffu, nch, src);
-        const long long exio = __shfl_sync(0xffffffffu, exi, src);
-        const long long exso = __shfl_sync(0xffffffffu, exs, src);
-        const long long l2 = local - exio;
-        const int cidx = (int)(l2 % ncho);
-        const long long rest = l2 / ncho;
-        const int rb = (int)(rest % p.n_rb);
-        const int g = (int)(rest / p.n_rb);
-        const int split = ncho > 1 ? (int)(split_off + exso + l2) : -1;
-        const int t0 = cidx * CH, t1 = min(nto, t0 + CH);
-        decode_item(bo, Po, g, rb, t0, t1, split);
-        next += gridDim.x;
-      }
-      item_off += win_items;
-      split_off += win_splits;
+    const int n_items = *reinterpret_cast<volatile int*>(&p.hdr->n_items);
+    while (ok) {
+      const int idx = grab();
+      if (idx >= n_items) break;
+      const int4 a = p.items[2 * idx], e = p.items[2 * idx + 1];
+      decode_item(a.x, e.z, a.y, a.z, e.x, e.y, a.w);
     }
   }
 
@@ -406,44 +343,29 @@ struct Planner {
   }
 
   // --------------------------------------------------------------------------
+  // Prefill items: index space (query tile, sequence, KV head, head pair),
+  // query tiles from the last (longest key range) down; empty ones skipped.
   __device__ void run_prefill() {
-    const int B = p.B, D = p.Dblk;
-    const int per_qt = p.Hkv * p.n_hp;
-    long long next = blockIdx.x, item_off = 0;
+    const int per_qt = p.B * p.Hkv * p.n_hp;
+    const int n_items = p.n_qt_max * per_qt;
     int bad = 0;
-    for (int b0 = 0; b0 < B && ok; b0 += 32) {
-      const int b = b0 + lane;
-      int start = 0, T = 0;
-      long long items = 0;
-      if (b < B) {
-        start = __ldg(p.lens + b);
-        const int end = __ldg(p.lens + b + 1);
-        T = end - start;
-        if (start < 0 || T < 0 || end > p.dense_tokens) {
-          bad = 1;
-          T = 0;
-        }
-        items = (long long)ceil_div(T, kRowsPerMTile) * per_qt;
+    while (ok) {
+      const int idx = grab();
+      if (idx >= n_items) break;
+      const int qt = p.n_qt_max - 1 - idx / per_qt;
+      const int rest = idx % per_qt;
+      const int b = rest / (p.Hkv * p.n_hp);
+      const int g = (rest / p.n_hp) % p.Hkv, hp = rest % p.n_hp;
+      const int start = __ldg(p.lens + b), end = __ldg(p.lens + b + 1);
+      int T = end - start;
+      if (start < 0 || T < 0 || end > p.dense_tokens) {
+        bad = 1;
+        T = 0;
       }
-      const long long exi = warp_excl_scan_ll(items, lane);
-      const long long win_items = warp_sum_ll(items);
-      while (ok && next < item_off + win_items) {
-        const long long local = next - item_off;
-        const unsigned own = __ballot_sync(0xffffffffu, b < B && local >= exi && local < exi + items);
-        const int src = __ffs(own) - 1;
-        const int so = __shfl_sync(0xffffffffu, start, src);
-        const int To = __shfl_sync(0xffffffffu, T, src);
-        const long long l2 = local - __shfl_sync(0xffffffffu, exi, src);
-        const int n_qt = ceil_div(To, kRowsPerMTile);
-        const int qt = n_qt - 1 - (int)(l2 / per_qt);  // longest rows first
-        const int rest = (int)(l2 % per_qt);
-        const int g = rest / p.n_hp, hp = rest % p.n_hp;
-        prefill_item(so, To, qt, g, hp, D);
-        next += gridDim.x;
-      }
-      item_off += win_items;
+      if (qt * kRowsPerMTile >= T) continue;
+      prefill_item(start, T, qt, g, hp, p.Dblk);
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, kErrBadLength);
+    if (bad && lane == 0) record_error(p, kErrBadLength);
   }
 
   __device__ void prefill_item(int start, int T, int qt, int g, int hp, int D) {
@@ -476,42 +398,27 @@ struct Planner {
     return p.live_pos ? __ldg(p.live_pos + (size_t)b * p.max_live + r) : p.prompt_len + r;
   }
 
+  // Multicanvas items: index space (row block, sequence, KV head).
   __device__ void run_multicanvas() {
-    const int B = p.B;
     const int rows_per_item = 2 * p.tpm;
-    long long next = blockIdx.x, item_off = 0;
+    const int n_items = p.n_rb_max * p.B * p.Hkv;
     int bad = 0;
-    for (int b0 = 0; b0 < B && ok; b0 += 32) {
-      const int b = b0 + lane;
-      int n_live = 0, A = 0;
-      long long items = 0;
-      if (b < B) {
-        n_live = p.lens ? __ldg(p.lens + b) : p.max_live;
-        A = __ldg(p.arena_len + b);
-        if (n_live < 0 || n_live > p.max_live || A < 0 || (long long)A > (long long)p.max_pages * p.S) {
-          bad = 1;
-          n_live = 0;
-          A = 0;
-        }
-        items = (long long)ceil_div(n_live, rows_per_item) * p.Hkv;
+    while (ok) {
+      const int idx = grab();
+      if (idx >= n_items) break;
+      const int rb = idx / (p.B * p.Hkv);
+      const int b = (idx / p.Hkv) % p.B, g = idx % p.Hkv;
+      int n_live = p.lens ? __ldg(p.lens + b) : p.max_live;
+      int A = __ldg(p.arena_len + b);
+      if (n_live < 0 || n_live > p.max_live || A < 0 ||
+          (long long)A > (long long)p.max_pages * p.S) {
+        bad = 1;
+        continue;
       }
-      const long long exi = warp_excl_scan_ll(items, lane);
-      const long long win_items = warp_sum_ll(items);
-      while (ok && next < item_off + win_items) {
-        const long long local = next - item_off;
-        const unsigned own = __ballot_sync(0xffffffffu, b < B && local >= exi && local < exi + items);
-        const int src = __ffs(own) - 1;
-        const int bo = b0 + src;
-        const int nlo = __shfl_sync(0xffffffffu, n_live, src);
-        const int Ao = __shfl_sync(0xffffffffu, A, src);
-        const long long l2 = local - __shfl_sync(0xffffffffu, exi, src);
-        const int rb = (int)(l2 / p.Hkv), g = (int)(l2 % p.Hkv);
-        multicanvas_item(bo, nlo, Ao, g, rb);
-        next += gridDim.x;
-      }
-      item_off += win_items;
+      if (rb * rows_per_item >= n_live) continue;
+      multicanvas_item(b, n_live, A, g, rb);
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, kErrBadLength);
+    if (bad && lane == 0) record_error(p, kErrBadLength);
   }
 
   // Classify one arena tile (entries [64a, 64a+64) of sequence b):
@@ -756,12 +663,12 @@ __device__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap*
 // MMA issuer (warp 1, one thread)
 // ============================================================================
 template <int HD>
-__device__ __forceinline__ void issue_qk(const Ctx& c, int m, uint32_t slot) {
+__device__ __forceinline__ void issue_qk(const Ctx& c, int m, int sb, uint32_t slot) {
   using C = Cfg<HD>;
   constexpr uint32_t idesc = make_idesc_bf16(128, kTileKeys, 0, 0);
   const uint32_t qa = smem_u32(c.smem + C::kOffQ + m * C::kQBytes);
   const uint32_t ka = smem_u32(c.smem + C::kOffKV + slot * C::kSlotBytes);
-  const uint32_t d = c.tmem + C::kColS + m * kTileKeys;
+  const uint32_t d = c.tmem + C::kColS + (2 * m + sb) * kTileKeys;
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks) {
     const int h = ks >> 2, kin = ks & 3;
@@ -786,10 +693,16 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int m, uint32_t slot, boo
   }
 }
 
+// Issue order for an item of n tiles (K(t), V(t) are loads 2t, 2t+1 of the
+// item):   S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... | PV(n-1)
+// where S(t) = Q K(t)^T for every active M-tile into S buffer t%2 and
+// PV(t) = P(t) V(t) accumulated into O.  The S of tile t+2 is computed while
+// the softmax warps work on tile t+1.
 template <int HD>
-__device__ void run_mma(const Ctx& c, const AttnParams& p, int lane) {
+__device__ void run_mma(const Ctx& c, const AttnParams& p) {
   using C = Cfg<HD>;
   uint32_t ri = 0, u = 0, qn[2] = {0, 0}, pn[2] = {0, 0}, on[2] = {0, 0};
+  uint32_t sn[2][2] = {{0, 0}, {0, 0}};  // S issued per (M-tile, buffer)
   bool ok = true;
   while (ok) {
     const Rec* r = ring_get1(c, p, ri);
@@ -798,63 +711,58 @@ __device__ void run_mma(const Ctx& c, const AttnParams& p, int lane) {
     ring_release1(c, ri);
     ++ri;
     if (kind == kRecEnd) break;
-    // kind == item
     for (int m = 0; m < n_m && ok; ++m) {
       ok = wait_bar(c, p, &c.bar.q_full[m], qn[m] & 1);
       ++qn[m];
     }
     if (!ok) break;
-    tc_fence_after();
-    // tile 0: S = Q K^T for every active M-tile
-    if (!ring_get1(c, p, ri)) break;
-    ring_release1(c, ri);
-    ++ri;
-    uint32_t ks = u % C::kStages;
-    if (!wait_bar(c, p, &c.bar.kv_full[ks], (u / C::kStages) & 1)) break;
-    ++u;
-    tc_fence_after();
-    for (int m = 0; m < n_m; ++m) {
-      issue_qk<HD>(c, m, ks);
-      umma_commit(&c.bar.s_full[m]);
-      if (n_t == 1) umma_commit(&c.bar.q_empty[m]);
-    }
-    umma_commit(&c.bar.kv_empty[ks]);
-    for (int j = 0; j < n_t && ok; ++j) {
-      const uint32_t vs = u % C::kStages;
-      if (!(ok = wait_bar(c, p, &c.bar.kv_full[vs], (u / C::kStages) & 1))) break;
-      ++u;
-      tc_fence_after();
-      const bool nxt = j + 1 < n_t;
-      if (nxt) {
-        if (!(ok = ring_get1(c, p, ri) != nullptr)) break;
-        ring_release1(c, ri);
-        ++ri;
+    const uint32_t ub = u;
+    u += 2u * (uint32_t)n_t;
+
+    // S(t) for every active M-tile
+    auto issue_s = [&](int t) -> bool {
+      if (!ring_get1(c, p, ri)) return false;  // tile record t (content not needed here)
+      ring_release1(c, ri);
+      ++ri;
+      const uint32_t uk = ub + 2u * (uint32_t)t;
+      const uint32_t ks = uk % C::kStages;
+      if (!wait_bar(c, p, &c.bar.kv_full[ks], (uk / C::kStages) & 1)) return false;
+      const int sb = t & 1;
+      for (int m = 0; m < n_m; ++m) {
+        if (sn[m][sb] > 0 &&
+            !wait_bar(c, p, &c.bar.s_free[2 * m + sb], (sn[m][sb] - 1) & 1))
+          return false;
+        tc_fence_after();
+        issue_qk<HD>(c, m, sb, ks);
+        umma_commit(&c.bar.s_full[2 * m + sb]);
+        ++sn[m][sb];
+        if (t == n_t - 1) umma_commit(&c.bar.q_empty[m]);  // last read of Q
       }
+      umma_commit(&c.bar.kv_empty[ks]);
+      return true;
+    };
+
+    ok = issue_s(0);
+    if (ok && n_t > 1) ok = issue_s(1);
+    for (int j = 0; j < n_t && ok; ++j) {
+      const uint32_t uv = ub + 2u * (uint32_t)j + 1u;
+      const uint32_t vs = uv % C::kStages;
+      if (!(ok = wait_bar(c, p, &c.bar.kv_full[vs], (uv / C::kStages) & 1))) break;
       for (int m = 0; m < n_m && ok; ++m) {
         if (!(ok = wait_bar(c, p, &c.bar.p_full[m], pn[m] & 1))) break;
         ++pn[m];
-        if (j == 0) {
-          if (!(ok = wait_bar(c, p, &c.bar.o_empty[m], (on[m] & 1) ^ 1))) break;
-        }
+        if (j == 0 && !(ok = wait_bar(c, p, &c.bar.o_empty[m], (on[m] & 1) ^ 1))) break;
         tc_fence_after();
         issue_pv<HD>(c, m, vs, j > 0);
-        if (m == n_m - 1) umma_commit(&c.bar.kv_empty[vs]);
-        if (nxt) {
-          if (m == 0) {
-            ks = u % C::kStages;
-            if (!(ok = wait_bar(c, p, &c.bar.kv_full[ks], (u / C::kStages) & 1))) break;
-            ++u;
-            tc_fence_after();
-          }
-          issue_qk<HD>(c, m, ks);
-          umma_commit(&c.bar.s_full[m]);
-          if (j + 2 == n_t) umma_commit(&c.bar.q_empty[m]);
-          if (m == n_m - 1) umma_commit(&c.bar.kv_empty[ks]);
-        } else {
+        umma_commit(&c.bar.pv_done[m]);
+        if (j == n_t - 1) {
           umma_commit(&c.bar.o_full[m]);
           ++on[m];
         }
       }
+      if (!ok) break;
+      umma_commit(&c.bar.kv_empty[vs]);
+      if (j + 2 < n_t) ok = issue_s(j + 2);
     }
   }
   // teardown: wait until every MMA issued by this thread has completed
@@ -870,11 +778,12 @@ __device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, in
   using C = Cfg<HD>;
   const int r = 32 * wq + lane;  // row within the M-tile == TMEM lane
   const uint32_t lane_addr = static_cast<uint32_t>(32 * wq) << 16;
-  const uint32_t t_s = c.tmem + lane_addr + C::kColS + m * kTileKeys;
   const uint32_t t_o = c.tmem + lane_addr + C::kColO + m * HD;
   const uint32_t p_row = smem_u32(c.smem + C::kOffP + m * C::kPBytes) + r * 128;
   const uint32_t sw = r & 7;
-  uint32_t ri = 0, sn = 0, on = 0;
+  const float sl2 = p.scale_log2;
+  uint32_t ri = 0, on = 0, pvn = 0;
+  uint32_t sc[2] = {0, 0};  // S consumed per buffer
   while (true) {
     const Rec* rec = ring_get(c, p, ri);
     if (!rec) return;
@@ -906,16 +815,21 @@ __device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, in
       ring_release(c, ri, lane);
       ++ri;
       if (!active) continue;
-      if (!wait_bar_warp(c, p, &c.bar.s_full[m], sn & 1)) return;
-      ++sn;
+      const int sb = j & 1;
+      if (!wait_bar_warp(c, p, &c.bar.s_full[2 * m + sb], sc[sb] & 1)) return;
+      ++sc[sb];
       tc_fence_after();
       uint32_t s0[32], s1[32];
-      tmem_ld64_sync(t_s, s0, s1);
+      tmem_ld64_sync(c.tmem + lane_addr + C::kColS + (2 * m + sb) * kTileKeys, s0, s1);
+      // the S buffer may now be overwritten by the S of tile j+2
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.bar.s_free[2 * m + sb]);
       float x[64];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        x[k] = __uint_as_float(s0[k]) * p.scale_log2;
-        x[k + 32] = __uint_as_float(s1[k]) * p.scale_log2;
+        x[k] = __uint_as_float(s0[k]);
+        x[k + 32] = __uint_as_float(s1[k]);
       }
       if (!full) {
 #pragma unroll
@@ -929,18 +843,44 @@ __device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, in
           if (!(kp < lim)) x[k] = -INFINITY;
         }
       }
-      float mt = x[0];
+      // row maximum of the raw scores (the scale is positive), in log2 units
+      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-      for (int k = 1; k < 64; ++k) mt = fmaxf(mt, x[k]);
+      for (int k = 4; k < 64; k += 4) {
+        mx0 = fmaxf(mx0, x[k]);
+        mx1 = fmaxf(mx1, x[k + 1]);
+        mx2 = fmaxf(mx2, x[k + 2]);
+        mx3 = fmaxf(mx3, x[k + 3]);
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       const float m_new = fmaxf(m_run, mt);
+      bool rescale = false;
+      float alpha = 1.0f;
       if (j == 0) {
         m_run = m_new;
-      } else {
-        const bool need = m_new > m_run + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          // O holds the PV products of earlier tiles (complete: the S commit
-          // of this tile was issued after them); rescale it in TMEM.
-          const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+      } else if (m_new > m_run + kRescaleThreshold) {
+        // lazy rescaling: only when the running maximum grows by more than 2^8
+        rescale = true;
+        alpha = ex2_approx(m_run - m_new);
+        m_run = m_new;
+      }
+      const float ref = m_run == -INFINITY ? 0.f : m_run;
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t w[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float p0 = ex2_approx(fmaf(x[2 * k], sl2, -ref));
+        const float p1 = ex2_approx(fmaf(x[2 * k + 1], sl2, -ref));
+        sum0 += p0;
+        sum1 += p1;
+        w[k] = pack_bf16x2(p0, p1);
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      if (j > 0) {
+        // P buffer and O are still in use by the PV of tile j-1 until it completes
+        if (!wait_bar_warp(c, p, &c.bar.pv_done[m], (pvn - 1) & 1)) return;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
           for (int c0 = 0; c0 < HD; c0 += 32) {
             uint32_t o[32];
@@ -950,29 +890,17 @@ __device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, in
             tmem_st32(t_o + c0, o);
           }
           tmem_st_wait();
-          l_run *= alpha;
-          if (need) m_run = m_new;
         }
       }
-      const float ref = m_run == -INFINITY ? 0.f : m_run;
-      float sum = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2_approx(x[8 * cc + 2 * k] - ref);
-          const float p1 = ex2_approx(x[8 * cc + 2 * k + 1] - ref);
-          sum += p0 + p1;
-          w[k] = pack_bf16x2(p0, p1);
-        }
-        st_shared_v4(p_row + ((cc ^ sw) << 4), w[0], w[1], w[2], w[3]);
-      }
-      l_run += sum;
+      for (int cc = 0; cc < 8; ++cc)
+        st_shared_v4(p_row + ((cc ^ sw) << 4), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2],
+                     w[4 * cc + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.bar.p_full[m]);
+      ++pvn;
     }
     if (!active) continue;
     if (!wait_bar_warp(c, p, &c.bar.o_full[m], on & 1)) return;
@@ -1052,8 +980,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.bar.q_full = c.bar.kv_empty + C::kStages;
   c.bar.q_empty = c.bar.q_full + 2;
   c.bar.s_full = c.bar.q_empty + 2;
-  c.bar.p_full = c.bar.s_full + 2;
-  c.bar.o_full = c.bar.p_full + 2;
+  c.bar.s_free = c.bar.s_full + 4;
+  c.bar.p_full = c.bar.s_free + 4;
+  c.bar.pv_done = c.bar.p_full + 2;
+  c.bar.o_full = c.bar.pv_done + 2;
   c.bar.o_empty = c.bar.o_full + 2;
   c.bar.drain = c.bar.o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -1071,10 +1001,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 0; m < 2; ++m) {
       mbar_init(&c.bar.q_full[m], 1);
       mbar_init(&c.bar.q_empty[m], 1);
-      mbar_init(&c.bar.s_full[m], 1);
       mbar_init(&c.bar.p_full[m], 4);
+      mbar_init(&c.bar.pv_done[m], 1);
       mbar_init(&c.bar.o_full[m], 1);
       mbar_init(&c.bar.o_empty[m], 4);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&c.bar.s_full[2 * m + b], 1);
+        mbar_init(&c.bar.s_free[2 * m + b], 4);
+      }
     }
     mbar_init(c.bar.drain, 1);
     *c.abort_flag = 0;
@@ -1102,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 0) {
     run_loader<HD>(c, p, &tm_q, &tm_kp, &tm_vp, &tm_kd, &tm_vd, lane);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<HD>(c, p, lane);
+    if (lane == 0) run_mma<HD>(c, p);
   } else if (warp >= 4) {
     run_softmax<HD>(c, p, (warp - 4) >> 2, warp & 3, lane);
   }

@@ -19,8 +19,9 @@ enum Mode : int { kModeDecode = 0, kModePrefill = 1, kModeMulticanvas = 2 };
 // First 256 bytes of every workspace.
 struct WsHeader {
   int32_t status;          // first device-detected error (0 = none)
-  int32_t chunk_tiles;     // decode: KV tiles per split chunk chosen by the planner
-  int32_t reserved0[2];
+  int32_t chunk_tiles;     // decode: KV tiles per split chunk chosen by the plan kernel
+  int32_t n_items;         // work items of the current call
+  int32_t work_next;       // next work item to hand out (reset by the plan kernel)
   unsigned long long tiles_full;
   unsigned long long tiles_partial;
   unsigned long long tiles_skipped;
@@ -29,14 +30,18 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header size");
 constexpr size_t kWsHeaderBytes = 256;
 
-// Decode workspace: header | split_base int32[B] (256-aligned) | partial
-// (max, sum) float2[cap][256] | partial O float[cap][d/4][256][4].
+// Decode workspace: header | split_base int32[B] | item list int4[2][items_cap]
+// | partial (max, sum) float2[cap][256] | partial O float[cap][d/4][256][4]
+// (regions 256-byte aligned).  items_cap bounds the number of work items
+// (n_sms * waves + B * Hkv * n_rb); cap (split-KV slots) is whatever fits.
 struct DecodeWsLayout {
-  size_t split_base_off, ml_off, o_off, bytes_per_slot;
+  size_t split_base_off, items_off, ml_off, o_off, bytes_per_slot;
+  int items_cap;
   int cap;
 };
-DecodeWsLayout decode_ws_layout(int B, int head_dim, size_t ws_bytes);
+DecodeWsLayout decode_ws_layout(int B, int Hkv, int n_rb, int head_dim, int n_sms, size_t ws_bytes);
 size_t decode_ws_recommended(int B, int Hkv, int n_rb, int head_dim, int n_sms);
+size_t decode_ws_minimum(int B, int Hkv, int n_rb, int head_dim, int n_sms);
 
 struct AttnParams {
   int mode;
@@ -46,6 +51,8 @@ struct AttnParams {
   int n_hp;            // prefill: M-tile pairs (heads) per KV head
   int n_rb;            // decode: row blocks per KV head (each = 2 M-tiles)
   int ch_min, waves;   // decode split policy
+  int n_qt_max;        // prefill: query tiles of the longest sequence (host bound)
+  int n_rb_max;        // multicanvas: row blocks of the longest live list (host bound)
   float scale_log2;    // softmax scale * log2(e)
   const int32_t* page_table;
   const int32_t* lens;       // decode prefix_len | prefill cu_seqlens | multicanvas live_count
@@ -62,6 +69,8 @@ struct AttnParams {
   uint16_t* out;             // bf16 [q_tokens, Hq, d]
   WsHeader* hdr;
   int32_t* split_base;
+  int4* items;               // decode: item list written by the plan kernel
+  int items_cap;
   float* part_ml;
   float* part_o;
   int split_cap;
@@ -70,6 +79,10 @@ struct AttnParams {
 struct AttnMaps {
   CUtensorMap q, kp, vp, kd, vd;
 };
+
+// Plan kernel: resets the work counter; for decode also chooses the split
+// chunk, orders sequences longest first and writes the item list.
+cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream);
 
 // Launch the block-causal attention kernel (decode, prefill or multicanvas).
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head_dim, int grid,

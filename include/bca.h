@@ -82,6 +82,7 @@ extern "C" {
 #define BCA_OP_PREFILL 2
 #define BCA_OP_MULTICANVAS 3
 #define BCA_OP_COMMIT 4
+#define BCA_OP_DECODE_MIN 5 /* smallest decode workspace: no split-KV partials */
 
 /* Shared dimensions of one call.  `version` must be BCA_ABI_VERSION. */
 typedef struct bca_dims {
@@ -107,10 +108,11 @@ int bca_version(void);
 const char* bca_status_string(int status);
 
 /* Bytes of workspace `op` needs for these dims, or 0 if the dims are invalid.
- * Decode: a status header, a per-sequence table and fp32 partial results for
- * splitting long prefixes across CTAs (split-KV); any size >= the value
- * returned for a smaller batch still works, with less splitting.  Other ops
- * need only the header. */
+ * Decode: a status header, a per-sequence table, the work-item list and fp32
+ * partial results for splitting long prefixes across CTAs (split-KV).  Any
+ * size between BCA_OP_DECODE_MIN (no partials: long prefixes are then not
+ * split) and BCA_OP_DECODE (the recommended size) works; the plan kernel
+ * splits only as far as the partials fit.  Other ops need only the header. */
 size_t bca_workspace_size(const bca_dims* dims, int op);
 
 /* Zero the workspace header (status word, counters).  Call once after
@@ -250,7 +252,8 @@ int bca_validate_page_table(const bca_dims* dims, const int32_t* page_table_host
 #define BCA_KERNEL_COMBINE 1   /* split-KV combine (decode) */
 #define BCA_KERNEL_COMMIT 2    /* KV commit / prefill page write */
 #define BCA_KERNEL_PROMOTE 3   /* multicanvas arena promotion */
-#define BCA_KERNEL_KINDS 4
+#define BCA_KERNEL_PLAN 4      /* work planning before each attention launch */
+#define BCA_KERNEL_KINDS 5
 
 typedef struct bca_kernel_times {
   int32_t launches[BCA_KERNEL_KINDS];

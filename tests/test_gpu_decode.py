@@ -94,7 +94,9 @@ def test_split_kv_matches_unsplit(cuda_lib):
     a = r.run().clone()
     assert_close(a, ref, what="split")
     import block_causal_paged_gb300 as bca
-    small = torch.empty(4096, dtype=torch.uint8, device="cuda")  # header + table only
+    n = bca.workspace_size(r.d, bca.OP_DECODE_MIN)   # no room for split-KV partials
+    assert 0 < n < bca.workspace_size(r.d, bca.OP_DECODE)
+    small = torch.empty(n, dtype=torch.uint8, device="cuda")
     bca.workspace_init(small)
     b = r.run(ws=small).clone()
     assert bca.read_device_status(small) == 0

@@ -1,0 +1,91 @@
+"""GPU parity of bca_multicanvas (live rows over an arena) and its promotion."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _gpu_cases import MulticanvasRun, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _ref(c):
+    return oracle.multicanvas(c.q_live, c.k_live, c.v_live, c.live_pos, c.live_count, c.arena_k,
+                              c.arena_v, c.arena_pos, c.prompt_len, c.canvas_len)
+
+
+def _live_mask(c):
+    n = c.q_live.shape[1]
+    return (np.arange(n)[None, :] < c.live_count.numpy()[:, None])
+
+
+def _expected_promotion(c):
+    S = c.pool.page_size
+    k = c.pool.k_pool.view(torch.int16).numpy().copy()
+    v = c.pool.v_pool.view(torch.int16).numpy().copy()
+    kv_pos = c.kv_pos.numpy().copy()
+    for b in range(c.B):
+        n = int(c.commit_count[b])
+        rows = c.commit_rows[b, :n].long()
+        A = int(c.arena_len[b])
+        pt = c.pool.page_table[b:b + 1]
+        k = oracle.commit(k, pt, [A], c.k_live[b, rows].view(torch.int16).numpy()[None], n, S)
+        v = oracle.commit(v, pt, [A], c.v_live[b, rows].view(torch.int16).numpy()[None], n, S)
+        for i in range(n):
+            e = A + i
+            kv_pos[int(pt[0, e // S]), e % S] = int(c.live_pos[b, int(rows[i])])
+    return k, v, kv_pos, (c.arena_len + c.commit_count).numpy()
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_multicanvas_b16(cuda_lib, seed):
+    """Batch 16, prompt 1024, 3 canvases of 256 with 30-100% live rows, 32/8
+    heads, d = 128; then 25% of each canvas's live rows are promoted."""
+    c = workloads.multicanvas_b16(seed=seed)
+    r = MulticanvasRun(c)
+    out = r.run()
+    assert r.status() == 0
+    m = _live_mask(c)
+    assert_close(out.cpu()[torch.from_numpy(m)], _ref(c)[m], what=f"multicanvas seed {seed}")
+    k, v, kv_pos, alen = _expected_promotion(c)
+    assert np.array_equal(r.k_pool.cpu().view(torch.int16).numpy(), k)
+    assert np.array_equal(r.v_pool.cpu().view(torch.int16).numpy(), v)
+    assert np.array_equal(r.kv_pos.cpu().numpy(), kv_pos)
+    assert np.array_equal(r.arena_len.cpu().numpy(), alen)
+
+
+def test_multicanvas_small_shapes(cuda_lib):
+    c = workloads.make_multicanvas_case(3, 40, 4, 24, Hq=6, Hkv=2, d=64, seed=5)
+    r = MulticanvasRun(c)
+    out = r.run()
+    assert r.status() == 0
+    m = _live_mask(c)
+    assert_close(out.cpu()[torch.from_numpy(m)], _ref(c)[m], what="small multicanvas")
+
+
+def test_live_order_equivariance(cuda_lib):
+    """Listing the live rows in another order permutes the outputs."""
+    a = workloads.make_multicanvas_case(2, 64, 3, 64, Hq=8, Hkv=2, d=128, seed=9)
+    b = workloads.make_multicanvas_case(2, 64, 3, 64, Hq=8, Hkv=2, d=128, seed=9,
+                                        shuffle_live=True)
+    oa = MulticanvasRun(a, promote=False).run().cpu()
+    ob = MulticanvasRun(b, promote=False).run().cpu()
+    for s in range(2):
+        n = int(a.live_count[s])
+        ia = {int(p): i for i, p in enumerate(a.live_pos[s, :n])}
+        for i, p in enumerate(b.live_pos[s, :n]):
+            err = (ob[s, i].float() - oa[s, ia[int(p)]].float()).abs().max()
+            assert err <= 2e-2
+
+
+def test_all_rows_live_one_canvas_is_block_decode(cuda_lib):
+    """With every row live and one canvas, the live-position list may be
+    omitted (row r at prompt_len + r) and the step equals a block decode."""
+    c = workloads.make_multicanvas_case(2, 128, 1, 64, Hq=8, Hkv=2, d=128, active_lo=1.0,
+                                        active_hi=1.0, seed=4)
+    r = MulticanvasRun(c, pass_positions=False, promote=False)
+    out = r.run()
+    assert r.status() == 0
+    ref = oracle.decode(c.q_live, c.k_live, c.v_live, c.arena_k, c.arena_v)
+    assert_close(out, ref, what="one canvas, all live")
