@@ -123,7 +123,7 @@ __device__ __forceinline__ void give_up(const Ctx& c, const AttnParams& p) {
 
 __device__ __forceinline__ bool wait_bar(const Ctx& c, const AttnParams& p, uint64_t* bar,
                                          uint32_t parity) {
-  if (mbar_wait(bar, parity, c.abort_flag, kWaitTimeoutNs)) return true;
+  if (mbar_wait(bar, parity, c.abort_flag, kWaitTimeoutCycles)) return true;
   give_up(c, p);
   return false;
 }
@@ -183,7 +183,7 @@ struct Planner {
   __device__ Planner(const AttnParams& p_, const Ctx& c_, int lane_) : p(p_), c(c_), lane(lane_) {}
 
   // Wait for a free ring entry; returns it (all lanes get the pointer).
-  __device__ Rec* acquire() {
+  __device__ __forceinline__ Rec* acquire() {
     const uint32_t slot = idx % kNumRec;
     if (!wait_bar_warp(c, p, &c.bar.rec_empty[slot], ((idx / kNumRec) & 1) ^ 1)) {
       ok = false;
@@ -206,7 +206,7 @@ struct Planner {
 
   // Emit one tile record.  coord[i]: per 16-key chunk, pool row / dense token
   // coordinate (already out of range for chunks with no valid key).
-  __device__ void emit_tile(int src, int full, int nvalid, int head, int kmode, int kbase,
+  __device__ __forceinline__ void emit_tile(int src, int full, int nvalid, int head, int kmode, int kbase,
                             const int (&coord)[4], const int (&koff)[4]) {
     Rec* r = acquire();
     if (!r) return;
@@ -228,7 +228,7 @@ struct Planner {
     if (full) ++n_full; else ++n_partial;
   }
 
-  __device__ void emit_item(int n_tiles, int n_m, int qmode, const int (&qtok)[2],
+  __device__ __forceinline__ void emit_item(int n_tiles, int n_m, int qmode, const int (&qtok)[2],
                             const int (&qhead)[2], const int (&ntok)[2], const int (&qbase)[2],
                             int P0, int Dblk, int split) {
     Rec* r = acquire();
@@ -238,6 +238,7 @@ struct Planner {
       r->w[I_NT] = n_tiles;
       r->w[I_NM] = n_m;
       r->w[I_QMODE] = qmode;
+#pragma unroll
       for (int m = 0; m < 2; ++m) {
         r->w[I_QTOK + m] = qtok[m];
         r->w[I_QHEAD + m] = qhead[m];
@@ -292,7 +293,7 @@ struct Planner {
   // starting at token coordinate tok0; key i has position kbase + i (kmode 0)
   // or live_pos[kbase + i] (kmode 2).  `min_lim` decides fully-included tiles
   // when positions are contiguous.
-  __device__ void emit_dense_tile(int g, int tok0, int nvalid, int kmode, int kbase, int full) {
+  __device__ __forceinline__ void emit_dense_tile(int g, int tok0, int nvalid, int kmode, int kbase, int full) {
     int cd[4], ko[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int i = 0; i < 4; ++i) cd[i] = (i * kChunkKeys < nvalid) ? tok0 + i * kChunkKeys : p.dense_tokens;
@@ -322,6 +323,7 @@ struct Planner {
   __device__ void decode_item(int b, int P, int g, int rb, int t0, int t1, int split) {
     const int D = p.Dblk;
     int qtok[2], qhead[2], ntok[2], qbase[2];
+#pragma unroll
     for (int m = 0; m < 2; ++m) {
       const int tok = rb * 2 * p.tpm + m * p.tpm;
       ntok[m] = max(0, min(p.tpm, D - tok));
@@ -495,6 +497,7 @@ struct Planner {
     for (int l = 0; l < n_lt; ++l)
       if (live_tile(b, n_live, l, min_lim, max_lim) != 0) ++n_tiles;
     int qtok[2], qhead[2], ntok[2], qbase[2];
+#pragma unroll
     for (int m = 0; m < 2; ++m) {
       const int r = r0 + m * p.tpm;
       ntok[m] = max(0, min(p.tpm, n_live - r));
@@ -559,13 +562,14 @@ __device__ __forceinline__ void ring_release1(const Ctx& c, uint32_t i) {
 // loader (warp 0)
 // ============================================================================
 template <int HD>
-__device__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap* tm_q,
+__device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap* tm_q,
                            const CUtensorMap* tm_kp, const CUtensorMap* tm_vp,
                            const CUtensorMap* tm_kd, const CUtensorMap* tm_vd, int lane) {
   using C = Cfg<HD>;
   const uint32_t q_base = smem_u32(c.smem + C::kOffQ);
   const uint32_t kv_base = smem_u32(c.smem + C::kOffKV);
-  uint32_t ri = 0, u = 0, qn[2] = {0, 0};
+  // phase bits (bit m): Q loads issued per M-tile (parity) and whether any
+  uint32_t ri = 0, u = 0, q_par = 0, q_used = 0;
   bool ok = true;
   while (ok) {
     const Rec* r = ring_get(c, p, ri);
@@ -579,8 +583,10 @@ __device__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap*
     if (kind == kRecEnd) break;
     if (kind == kRecItem) {
       const int n_m = f[I_NM];
-      for (int m = 0; m < n_m; ++m) {
-        if (!wait_bar_warp(c, p, &c.bar.q_empty[m], (qn[m] & 1) ^ 1)) { ok = false; break; }
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        if (m >= n_m) break;
+        if (!wait_bar_warp(c, p, &c.bar.q_empty[m], ((q_par >> m) & 1) ^ 1)) { ok = false; break; }
         if (lane == 0) {
           // the Q box holds hpr x tpm rows (126 for G = 3), 128 bytes per row per half
           mbar_arrive_expect_tx(&c.bar.q_full[m], (uint32_t)(C::kHalves * p.hpr * p.tpm * 128));
@@ -590,7 +596,8 @@ __device__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap*
                         f[I_QHEAD + m], f[I_QTOK + m]);
         }
         __syncwarp();
-        ++qn[m];
+        q_par ^= 1u << m;
+        q_used |= 1u << m;
       }
       continue;
     }
@@ -653,10 +660,12 @@ __device__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap*
   // teardown: never leave this CTA with copies in flight
   for (uint32_t k = 0; k < (uint32_t)C::kStages && k < u; ++k) {
     const uint32_t uu = u - 1 - k;
-    mbar_wait(&c.bar.kv_full[uu % C::kStages], (uu / C::kStages) & 1, c.abort_flag, kWaitTimeoutNs);
+    mbar_wait(&c.bar.kv_full[uu % C::kStages], (uu / C::kStages) & 1, c.abort_flag, kWaitTimeoutCycles);
   }
+#pragma unroll
   for (int m = 0; m < 2; ++m)
-    if (qn[m]) mbar_wait(&c.bar.q_full[m], (qn[m] - 1) & 1, c.abort_flag, kWaitTimeoutNs);
+    if ((q_used >> m) & 1)
+      mbar_wait(&c.bar.q_full[m], ((q_par >> m) & 1) ^ 1, c.abort_flag, kWaitTimeoutCycles);
 }
 
 // ============================================================================
@@ -699,10 +708,12 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int m, uint32_t slot, boo
 // PV(t) = P(t) V(t) accumulated into O.  The S of tile t+2 is computed while
 // the softmax warps work on tile t+1.
 template <int HD>
-__device__ void run_mma(const Ctx& c, const AttnParams& p) {
+__device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
   using C = Cfg<HD>;
-  uint32_t ri = 0, u = 0, qn[2] = {0, 0}, pn[2] = {0, 0}, on[2] = {0, 0};
-  uint32_t sn[2][2] = {{0, 0}, {0, 0}};  // S issued per (M-tile, buffer)
+  // Phase parities kept as bits so that no counter array needs memory:
+  // bit m of q_par/p_par/o_par for M-tile m; bit 2m+b of s_par/s_used for
+  // S buffer b of M-tile m.
+  uint32_t ri = 0, u = 0, q_par = 0, p_par = 0, o_par = 0, s_par = 0, s_used = 0;
   bool ok = true;
   while (ok) {
     const Rec* r = ring_get1(c, p, ri);
@@ -711,9 +722,12 @@ __device__ void run_mma(const Ctx& c, const AttnParams& p) {
     ring_release1(c, ri);
     ++ri;
     if (kind == kRecEnd) break;
-    for (int m = 0; m < n_m && ok; ++m) {
-      ok = wait_bar(c, p, &c.bar.q_full[m], qn[m] & 1);
-      ++qn[m];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      if (m < n_m && ok) {
+        ok = wait_bar(c, p, &c.bar.q_full[m], (q_par >> m) & 1);
+        q_par ^= 1u << m;
+      }
     }
     if (!ok) break;
     const uint32_t ub = u;
@@ -728,14 +742,18 @@ __device__ void run_mma(const Ctx& c, const AttnParams& p) {
       const uint32_t ks = uk % C::kStages;
       if (!wait_bar(c, p, &c.bar.kv_full[ks], (uk / C::kStages) & 1)) return false;
       const int sb = t & 1;
-      for (int m = 0; m < n_m; ++m) {
-        if (sn[m][sb] > 0 &&
-            !wait_bar(c, p, &c.bar.s_free[2 * m + sb], (sn[m][sb] - 1) & 1))
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        if (m >= n_m) break;
+        const int bi = 2 * m + sb;
+        if (((s_used >> bi) & 1) &&
+            !wait_bar(c, p, &c.bar.s_free[bi], ((s_par >> bi) & 1) ^ 1))
           return false;
         tc_fence_after();
         issue_qk<HD>(c, m, sb, ks);
-        umma_commit(&c.bar.s_full[2 * m + sb]);
-        ++sn[m][sb];
+        umma_commit(&c.bar.s_full[bi]);
+        s_par ^= 1u << bi;
+        s_used |= 1u << bi;
         if (t == n_t - 1) umma_commit(&c.bar.q_empty[m]);  // last read of Q
       }
       umma_commit(&c.bar.kv_empty[ks]);
@@ -748,16 +766,18 @@ __device__ void run_mma(const Ctx& c, const AttnParams& p) {
       const uint32_t uv = ub + 2u * (uint32_t)j + 1u;
       const uint32_t vs = uv % C::kStages;
       if (!(ok = wait_bar(c, p, &c.bar.kv_full[vs], (uv / C::kStages) & 1))) break;
-      for (int m = 0; m < n_m && ok; ++m) {
-        if (!(ok = wait_bar(c, p, &c.bar.p_full[m], pn[m] & 1))) break;
-        ++pn[m];
-        if (j == 0 && !(ok = wait_bar(c, p, &c.bar.o_empty[m], (on[m] & 1) ^ 1))) break;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        if (m >= n_m || !ok) break;
+        if (!(ok = wait_bar(c, p, &c.bar.p_full[m], (p_par >> m) & 1))) break;
+        p_par ^= 1u << m;
+        if (j == 0 && !(ok = wait_bar(c, p, &c.bar.o_empty[m], ((o_par >> m) & 1) ^ 1))) break;
         tc_fence_after();
         issue_pv<HD>(c, m, vs, j > 0);
         umma_commit(&c.bar.pv_done[m]);
         if (j == n_t - 1) {
           umma_commit(&c.bar.o_full[m]);
-          ++on[m];
+          o_par ^= 1u << m;
         }
       }
       if (!ok) break;
@@ -767,14 +787,14 @@ __device__ void run_mma(const Ctx& c, const AttnParams& p) {
   }
   // teardown: wait until every MMA issued by this thread has completed
   umma_commit(c.bar.drain);
-  mbar_wait(c.bar.drain, 0, c.abort_flag, kWaitTimeoutNs);
+  mbar_wait(c.bar.drain, 0, c.abort_flag, kWaitTimeoutCycles);
 }
 
 // ============================================================================
 // softmax / epilogue (warps 4..11)
 // ============================================================================
 template <int HD>
-__device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, int lane) {
+__device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, int lane) {
   using C = Cfg<HD>;
   const int r = 32 * wq + lane;  // row within the M-tile == TMEM lane
   const uint32_t lane_addr = static_cast<uint32_t>(32 * wq) << 16;
@@ -783,7 +803,7 @@ __device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, in
   const uint32_t sw = r & 7;
   const float sl2 = p.scale_log2;
   uint32_t ri = 0, on = 0, pvn = 0;
-  uint32_t sc[2] = {0, 0};  // S consumed per buffer
+  uint32_t s_par = 0;  // bit b: parity of the S phases consumed from buffer b
   while (true) {
     const Rec* rec = ring_get(c, p, ri);
     if (!rec) return;
@@ -816,8 +836,8 @@ __device__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, in
       ++ri;
       if (!active) continue;
       const int sb = j & 1;
-      if (!wait_bar_warp(c, p, &c.bar.s_full[2 * m + sb], sc[sb] & 1)) return;
-      ++sc[sb];
+      if (!wait_bar_warp(c, p, &c.bar.s_full[2 * m + sb], (s_par >> sb) & 1)) return;
+      s_par ^= 1u << sb;
       tc_fence_after();
       uint32_t s0[32], s1[32];
       tmem_ld64_sync(c.tmem + lane_addr + C::kColS + (2 * m + sb) * kTileKeys, s0, s1);

@@ -12,7 +12,8 @@ constexpr int kTileKeys = 64;     // keys per KV tile
 constexpr int kChunkKeys = 16;    // keys per TMA box (a page holds whole chunks)
 constexpr int kRowsPerMTile = 128;
 constexpr int kThreads = 384;     // 12 warps, see the role map in attention.cu
-constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s per internal wait
+// Per internal wait: about 2 s at the maximum SM clock (longer when clocked down).
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 enum Mode : int { kModeDecode = 0, kModePrefill = 1, kModeMulticanvas = 2 };
 

@@ -15,12 +15,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ uint32_t elect_lane0(uint32_t lane) { return lane == 0; }
 
 // ----------------------------------------------------------------------------
@@ -57,18 +51,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of the given parity to complete, for at most
-// `timeout_ns` of wall time.  Every few hundred polls the shared abort flag is
-// checked so that one role giving up releases all the others quickly.
-// Returns false on timeout or abort; the caller then skips to its teardown.
+// `timeout_cycles` SM clock cycles.  The clock is read only after 1024 failed
+// polls, so a wait that succeeds quickly costs nothing but the polls; the
+// shared abort flag is checked at the same cadence so that one role giving
+// up releases all the others.  Returns false on timeout or abort; the caller
+// then skips to its teardown.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t timeout_ns) {
+                                          long long timeout_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  long long t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u) {
+    if ((it & 1023u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) return false;
+      const long long now = clock64();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > timeout_cycles) return false;
     }
   }
 }
@@ -140,8 +138,7 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
@@ -149,8 +146,7 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
+          smem_u32(bar)));
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
