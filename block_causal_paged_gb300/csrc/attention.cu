@@ -3,7 +3,7 @@
 // One persistent CTA per SM takes work items from a shared counter (a small
 // plan kernel orders them longest first and resets the counter).  An item is a
 // block of up to 256 query rows (two M-tiles of 128 rows) that share one KV
-// head, plus the sequence of 64-key tiles those rows attend.  Rows are
+// head, plus the sequence of 128-key tiles those rows attend.  Rows are
 // (token, head) pairs: for decode and multicanvas the G query heads of one KV
 // head are packed into the rows (rows = tokens x G, so K/V is read once per
 // group); for prefill each M-tile is one head over 128 tokens.
@@ -23,13 +23,15 @@
 //   warp 0      loader   : TMA loads of Q and of K/V page boxes into a ring of
 //                          shared-memory stages (ragged 16-key chunks are
 //                          copied by the warp's lanes with zero fill)
-//   warp 1      MMA      : one thread issues tcgen05.mma: S = Q K^T into one of
-//                          two TMEM buffers per M-tile (S of tile j+2 is issued
-//                          while the softmax works on tile j), O += P V into TMEM
+//   warp 1      MMA      : one thread issues tcgen05.mma.  Per M-tile m and
+//                          tile j: O_m += P_m V_j with P_m read from TMEM, then
+//                          S_m = Q_m K_{j+1}^T into the same TMEM columns; the
+//                          two M-tiles alternate, so the tensor core works on
+//                          one while the softmax warps work on the other
 //   warp 2      TMEM allocation / release
 //   warps 4-7   softmax for M-tile 0, warps 8-11 for M-tile 1: read S rows
 //               from TMEM, mask, online softmax (lazy rescale of O), write P
-//               (bf16) to shared memory, final normalisation and store.
+//               (bf16) back into the S columns, final normalisation and store.
 // Every wait is bounded; on timeout the CTA records BCA_ERR_DEVICE_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
 #include <climits>
@@ -42,6 +44,10 @@ namespace bca {
 namespace {
 
 constexpr int kNumRec = 8;
+constexpr int kRegsLaunch = 168;   // 65536 / 384, rounded down to a multiple of 8
+constexpr int kRegsControl = 112;
+constexpr int kRegsSoftmax = 184;
+static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads, "register split");
 constexpr int kRecConsumers = 10;  // loader + MMA + 8 softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr int kErrTimeout = -18;
@@ -55,10 +61,10 @@ enum : int {
   I_KIND = 0, I_NT = 1, I_NM = 2, I_QMODE = 3, I_QTOK = 4 /*2*/, I_QHEAD = 6 /*2*/,
   I_NTOK = 8 /*2*/, I_QBASE = 10 /*2*/, I_P0 = 12, I_DBLK = 13, I_SPLIT = 14
 };
-// Tile fields:
+// Tile fields (one coordinate and one position offset per 16-key chunk):
 enum : int {
   T_KIND = 0, T_SRC = 1, T_FULL = 2, T_NVALID = 3, T_HEAD = 4, T_KMODE = 5, T_KBASE = 6,
-  T_COORD = 8 /*4*/, T_KOFF = 12 /*4*/
+  T_COORD = 8 /*8*/, T_KOFF = 16 /*8*/
 };
 struct __align__(16) Rec {
   int32_t w[32];
@@ -68,20 +74,20 @@ template <int HD>
 struct Cfg {
   static constexpr int kHalves = HD / 64;                 // 128-byte column blocks of a row
   static constexpr int kQBytes = kHalves * 16384;         // 128 rows of Q
-  static constexpr int kPBytes = 16384;                   // 128 rows x 64 keys of P (bf16)
-  static constexpr int kSlotBytes = kHalves * 8192;       // 64 keys of K or V
-  static constexpr int kStages = HD == 128 ? 7 : 14;
+  static constexpr int kHalfBytes = kTileKeys * 128;      // one 64-column half of a KV tile
+  static constexpr int kSlotBytes = kHalves * kHalfBytes; // 128 keys of K or V
+  static constexpr int kStages = HD == 128 ? 5 : 12;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;
-  static constexpr int kOffKV = kOffP + 2 * kPBytes;
+  static constexpr int kOffKV = kOffQ + 2 * kQBytes;
   static constexpr int kOffRec = kOffKV + kStages * kSlotBytes;
-  static constexpr int kNumBars = 2 * kNumRec + 2 * kStages + 20 + 1;
+  static constexpr int kNumBars = 2 * kNumRec + 2 * kStages + 12 + 1;
   static constexpr int kOffBar = kOffRec + kNumRec * (int)sizeof(Rec);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64;
   static constexpr int kSmemAlloc = kBytes + 1024;  // base is aligned up to 1024 in the kernel
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns: S of M-tile m, buffer b at 64*(2m+b); O of M-tile m at 256 + HD*m
+  // TMEM columns: S of M-tile m at 128*m (fp32, one column per key); P of
+  // M-tile m overwrites the first 64 of them (bf16 pairs); O at 256 + HD*m.
   static constexpr int kColS = 0;
   static constexpr int kColO = 256;
   static_assert(kColO + 2 * HD <= (int)kTmemCols, "TMEM plan");
@@ -95,10 +101,8 @@ struct Bars {
   uint64_t* kv_empty;
   uint64_t* q_full;    // [2]
   uint64_t* q_empty;   // [2]
-  uint64_t* s_full;    // [2 M-tiles][2 buffers]
-  uint64_t* s_free;    // [2][2]
+  uint64_t* s_full;    // [2]
   uint64_t* p_full;    // [2]
-  uint64_t* pv_done;   // [2]
   uint64_t* o_full;    // [2]
   uint64_t* o_empty;   // [2]
   uint64_t* drain;
@@ -206,8 +210,9 @@ struct Planner {
 
   // Emit one tile record.  coord[i]: per 16-key chunk, pool row / dense token
   // coordinate (already out of range for chunks with no valid key).
-  __device__ __forceinline__ void emit_tile(int src, int full, int nvalid, int head, int kmode, int kbase,
-                            const int (&coord)[4], const int (&koff)[4]) {
+  __device__ __forceinline__ void emit_tile(int src, int full, int nvalid, int head, int kmode,
+                                            int kbase, const int (&coord)[kChunksPerTile],
+                                            const int (&koff)[kChunksPerTile]) {
     Rec* r = acquire();
     if (!r) return;
     if (lane == 0) {
@@ -219,7 +224,7 @@ struct Planner {
       r->w[T_KMODE] = kmode;
       r->w[T_KBASE] = kbase;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kChunksPerTile; ++i) {
         r->w[T_COORD + i] = coord[i];
         r->w[T_KOFF + i] = koff[i];
       }
@@ -266,22 +271,26 @@ struct Planner {
   }
 
   // Emit the prefix tiles [t0, t1) of a decode/paged stream, keys 0..P-1 of
-  // sequence b, KV head g.  Page-table entries for 8 tiles are fetched at once.
+  // sequence b, KV head g.  Page-table entries for 4 tiles (32 chunks, one
+  // per lane) are fetched at once.
   __device__ void emit_pool_tiles_contig(int b, int g, int P, int t0, int t1) {
-    for (int tg = t0; tg < t1 && ok; tg += 8) {
-      // lane i: chunk i%4 of tile tg + i/4
-      const int t = tg + (lane >> 2);
-      const int k = t * kTileKeys + (lane & 3) * kChunkKeys;
+    constexpr int kTilesPerGroup = 32 / kChunksPerTile;
+    for (int tg = t0; tg < t1 && ok; tg += kTilesPerGroup) {
+      const int t = tg + lane / kChunksPerTile;
+      const int k = t * kTileKeys + (lane % kChunksPerTile) * kChunkKeys;
       int coord = p.pool_rows;  // out of range -> zero fill
       if (t < t1 && k < P) {
         const int page = page_of(b, k);
         if (page >= 0) coord = (page * p.Hkv + g) * p.S + (k % p.S);
       }
-      const int ntile = min(8, t1 - tg);
+      const int ntile = min(kTilesPerGroup, t1 - tg);
       for (int j = 0; j < ntile && ok; ++j) {
-        int cd[4], ko[4] = {0, 0, 0, 0};
+        int cd[kChunksPerTile], ko[kChunksPerTile];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cd[i] = __shfl_sync(0xffffffffu, coord, 4 * j + i);
+        for (int i = 0; i < kChunksPerTile; ++i) {
+          cd[i] = __shfl_sync(0xffffffffu, coord, kChunksPerTile * j + i);
+          ko[i] = 0;
+        }
         const int tt = tg + j;
         const int nvalid = min(kTileKeys, P - tt * kTileKeys);
         emit_tile(0, nvalid == kTileKeys, nvalid, g, 0, tt * kTileKeys, cd, ko);
@@ -289,14 +298,16 @@ struct Planner {
     }
   }
 
-  // Dense tiles: keys are rows [r0, r0+n) of a dense [tokens, Hkv, d] tensor
-  // starting at token coordinate tok0; key i has position kbase + i (kmode 0)
-  // or live_pos[kbase + i] (kmode 2).  `min_lim` decides fully-included tiles
-  // when positions are contiguous.
-  __device__ __forceinline__ void emit_dense_tile(int g, int tok0, int nvalid, int kmode, int kbase, int full) {
-    int cd[4], ko[4] = {0, 0, 0, 0};
+  // Dense tile: keys are tokens tok0.. of a dense [tokens, Hkv, d] tensor; key
+  // i has position kbase + i (kmode 0) or live_pos[kbase + i] (kmode 2).
+  __device__ __forceinline__ void emit_dense_tile(int g, int tok0, int nvalid, int kmode,
+                                                  int kbase, int full) {
+    int cd[kChunksPerTile], ko[kChunksPerTile];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) cd[i] = (i * kChunkKeys < nvalid) ? tok0 + i * kChunkKeys : p.dense_tokens;
+    for (int i = 0; i < kChunksPerTile; ++i) {
+      cd[i] = (i * kChunkKeys < nvalid) ? tok0 + i * kChunkKeys : p.dense_tokens;
+      ko[i] = 0;
+    }
     emit_tile(1, full, nvalid, g, kmode, kbase, cd, ko);
   }
 
@@ -423,13 +434,14 @@ struct Planner {
     if (bad && lane == 0) record_error(p, kErrBadLength);
   }
 
-  // Classify one arena tile (entries [64a, 64a+64) of sequence b):
-  // returns 0 skip, 1 partial, 2 full; fills coords/offsets on lane 0.
-  __device__ int arena_tile(int b, int A, int a, int g, int min_lim, int max_lim, int (&cd)[4],
-                            int (&ko)[4]) {
-    int kmin = INT_MAX, kmax = INT_MIN, pg[2];
+  // Classify one arena tile (entries [128a, 128a+128) of sequence b):
+  // returns 0 skip, 1 partial, 2 full; fills the chunk coordinates/offsets.
+  __device__ int arena_tile(int b, int A, int a, int g, int min_lim, int max_lim,
+                            int (&cd)[kChunksPerTile], int (&ko)[kChunksPerTile]) {
+    constexpr int kLoads = kTileKeys / 32;
+    int kmin = INT_MAX, kmax = INT_MIN, pg[kLoads];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kLoads; ++h) {
       const int e = a * kTileKeys + 32 * h + lane;
       pg[h] = -1;
       if (e < A) {
@@ -446,9 +458,9 @@ struct Planner {
     kmax = warp_max(kmax);
     const int nvalid = min(kTileKeys, A - a * kTileKeys);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      // chunk i starts at entry 16i: lane 16*(i&1) of load half i>>1
-      const int page = __shfl_sync(0xffffffffu, (i >> 1) ? pg[1] : pg[0], 16 * (i & 1));
+    for (int i = 0; i < kChunksPerTile; ++i) {
+      // chunk i starts at entry 16i: load i/2, lane 16*(i%2)
+      const int page = __shfl_sync(0xffffffffu, pg[i >> 1], 16 * (i & 1));
       const int e = a * kTileKeys + i * kChunkKeys;
       cd[i] = (e < A && page >= 0) ? (page * p.Hkv + g) * p.S + (e % p.S) : p.pool_rows;
       ko[i] = (e < A && page >= 0) ? page * p.S + (e % p.S) : 0;
@@ -461,7 +473,7 @@ struct Planner {
   __device__ int live_tile(int b, int n_live, int l, int min_lim, int max_lim) {
     int kmin = INT_MAX, kmax = INT_MIN;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kTileKeys / 32; ++h) {
       const int r = l * kTileKeys + 32 * h + lane;
       if (r < n_live) {
         const int pos = live_position(b, r);
@@ -491,7 +503,7 @@ struct Planner {
     // pass 1: count the tiles that are not fully excluded
     int n_tiles = 0;
     for (int a = 0; a < n_at; ++a) {
-      int cd[4], ko[4];
+      int cd[kChunksPerTile], ko[kChunksPerTile];
       if (arena_tile(b, A, a, g, min_lim, max_lim, cd, ko) != 0) ++n_tiles;
     }
     for (int l = 0; l < n_lt; ++l)
@@ -511,7 +523,7 @@ struct Planner {
     n_skip += (unsigned long long)(n_at + n_lt - n_tiles);
     // pass 2: emit
     for (int a = 0; a < n_at && ok; ++a) {
-      int cd[4], ko[4];
+      int cd[kChunksPerTile], ko[kChunksPerTile];
       const int cls = arena_tile(b, A, a, g, min_lim, max_lim, cd, ko);
       if (cls == 0) continue;
       emit_tile(0, cls == 2, min(kTileKeys, A - a * kTileKeys), g, 1, 0, cd, ko);
@@ -561,6 +573,16 @@ __device__ __forceinline__ void ring_release1(const Ctx& c, uint32_t i) {
 // ============================================================================
 // loader (warp 0)
 // ============================================================================
+// f[T_COORD + i] for a runtime i < kChunksPerTile, without indexing the array
+// dynamically (that would place it in local memory).
+__device__ __forceinline__ int coord_of(const int (&f)[24], int i) {
+  int v = 0;
+#pragma unroll
+  for (int k = 0; k < kChunksPerTile; ++k)
+    if (k == i) v = f[T_COORD + k];
+  return v;
+}
+
 template <int HD>
 __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap* tm_q,
                            const CUtensorMap* tm_kp, const CUtensorMap* tm_vp,
@@ -575,9 +597,9 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
     const Rec* r = ring_get(c, p, ri);
     if (!r) break;
     const int kind = r->w[0];
-    int f[16];
+    int f[24];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = r->w[i];
+    for (int i = 0; i < 24; ++i) f[i] = r->w[i];
     ring_release(c, ri, lane);
     ++ri;
     if (kind == kRecEnd) break;
@@ -601,8 +623,17 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
       }
       continue;
     }
-    // a KV tile: K then V, each into the next stage
+    // a KV tile: K then V, each into the next stage.  Lane l < 8 * halves
+    // copies one 16-key half-row box (chunk l / halves, half l % halves), so a
+    // tile's boxes go out as one warp instruction instead of one per box.
     const int src = f[T_SRC], nvalid = f[T_NVALID], head = f[T_HEAD];
+    const bool box_lane = lane < kChunksPerTile * C::kHalves;
+    const int my_chunk = box_lane ? lane / C::kHalves : 0;
+    const int my_half = lane % C::kHalves;
+    const int my_nv = min(max(nvalid - my_chunk * kChunkKeys, 0), kChunkKeys);
+    const int my_coord = __shfl_sync(0xffffffffu, lane < kChunksPerTile ? coord_of(f, lane) : 0,
+                                     my_chunk);
+    const bool my_tma = box_lane && (my_nv == 0 || my_nv == kChunkKeys);
     for (int kv = 0; kv < 2 && ok; ++kv) {
       const uint32_t slot = u % C::kStages;
       if (!wait_bar_warp(c, p, &c.bar.kv_empty[slot], ((u / C::kStages) & 1) ^ 1)) { ok = false; break; }
@@ -610,7 +641,7 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
       uint32_t tma_bytes = 0;
       bool manual = false;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kChunksPerTile; ++i) {
         const int nv = min(max(nvalid - i * kChunkKeys, 0), kChunkKeys);
         if (nv == 0 || nv == kChunkKeys) {
           tma_bytes += C::kHalves * 2048;
@@ -631,7 +662,8 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
             v = __ldg(reinterpret_cast<const uint4*>(base + row * HD + h * 64 + cc * 8));
           }
           const int krow = i * kChunkKeys + rr;
-          st_shared_v4(dst + h * 8192 + krow * 128 + ((cc ^ (krow & 7)) << 4), v.x, v.y, v.z, v.w);
+          st_shared_v4(dst + h * C::kHalfBytes + krow * 128 + ((cc ^ (krow & 7)) << 4), v.x, v.y,
+                       v.z, v.w);
         }
       }
       if (manual) fence_proxy_async_smem();
@@ -639,19 +671,14 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
       if (lane == 0) {
         if (tma_bytes) mbar_arrive_expect_tx(&c.bar.kv_full[slot], tma_bytes);
         else mbar_arrive(&c.bar.kv_full[slot]);
+      }
+      __syncwarp();
+      if (my_tma) {
+        // the planner made the coordinate out of range for a chunk with no key
         const CUtensorMap* map = src == 0 ? (kv ? tm_vp : tm_kp) : (kv ? tm_vd : tm_kd);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int nv = min(max(nvalid - i * kChunkKeys, 0), kChunkKeys);
-          if (nv != 0 && nv != kChunkKeys) continue;
-          const int coord = f[T_COORD + i];  // planner made it out of range if nv == 0
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            const uint32_t d = dst + h * 8192 + i * 2048;
-            if (src == 0) tma_load_2d(d, map, &c.bar.kv_full[slot], h * 64, coord);
-            else tma_load_3d(d, map, &c.bar.kv_full[slot], h * 64, head, coord);
-          }
-        }
+        const uint32_t d = dst + my_half * C::kHalfBytes + my_chunk * 2048;
+        if (src == 0) tma_load_2d(d, map, &c.bar.kv_full[slot], my_half * 64, my_coord);
+        else tma_load_3d(d, map, &c.bar.kv_full[slot], my_half * 64, head, my_coord);
       }
       __syncwarp();
       ++u;
@@ -671,49 +698,52 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
 // ============================================================================
 // MMA issuer (warp 1, one thread)
 // ============================================================================
+// S_m = Q_m K^T: M = 128 query rows, N = 128 keys, K = head_dim (16 per
+// instruction), both operands K-major in 128-byte-swizzled shared memory.
 template <int HD>
-__device__ __forceinline__ void issue_qk(const Ctx& c, int m, int sb, uint32_t slot) {
+__device__ __forceinline__ void issue_qk(const Ctx& c, int m, uint32_t slot) {
   using C = Cfg<HD>;
   constexpr uint32_t idesc = make_idesc_bf16(128, kTileKeys, 0, 0);
   const uint32_t qa = smem_u32(c.smem + C::kOffQ + m * C::kQBytes);
   const uint32_t ka = smem_u32(c.smem + C::kOffKV + slot * C::kSlotBytes);
-  const uint32_t d = c.tmem + C::kColS + (2 * m + sb) * kTileKeys;
+  const uint32_t d = c.tmem + C::kColS + m * kTileKeys;
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks) {
     const int h = ks >> 2, kin = ks & 3;
     const uint64_t a = make_sdesc_sw128(qa + h * 16384 + kin * 32, 16, 1024);
-    const uint64_t b = make_sdesc_sw128(ka + h * 8192 + kin * 32, 16, 1024);
+    const uint64_t b = make_sdesc_sw128(ka + h * C::kHalfBytes + kin * 32, 16, 1024);
     umma_bf16(d, a, b, idesc, ks > 0 ? 1u : 0u);
   }
 }
 
+// O_m (+)= P_m V: M = 128 rows, N = head_dim, K = 128 keys (16 per
+// instruction); P_m from TMEM (the S columns, 8 columns per 16 keys), V
+// MN-major in shared memory (LBO = the next 64 head-dim columns).
 template <int HD>
 __device__ __forceinline__ void issue_pv(const Ctx& c, int m, uint32_t slot, bool acc) {
   using C = Cfg<HD>;
   constexpr uint32_t idesc = make_idesc_bf16(128, HD, 0, 1);
-  const uint32_t pa = smem_u32(c.smem + C::kOffP + m * C::kPBytes);
+  const uint32_t pa = c.tmem + C::kColS + m * kTileKeys;
   const uint32_t va = smem_u32(c.smem + C::kOffKV + slot * C::kSlotBytes);
   const uint32_t d = c.tmem + C::kColO + m * HD;
 #pragma unroll
   for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-    const uint64_t a = make_sdesc_sw128(pa + ks * 32, 16, 1024);
-    const uint64_t b = make_sdesc_sw128(va + ks * 2048, 8192, 1024);
-    umma_bf16(d, a, b, idesc, (acc || ks > 0) ? 1u : 0u);
+    const uint64_t b = make_sdesc_sw128(va + ks * 2048, C::kHalfBytes, 1024);
+    umma_bf16_ts(d, pa + ks * 8, b, idesc, (acc || ks > 0) ? 1u : 0u);
   }
 }
 
 // Issue order for an item of n tiles (K(t), V(t) are loads 2t, 2t+1 of the
-// item):   S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... | PV(n-1)
-// where S(t) = Q K(t)^T for every active M-tile into S buffer t%2 and
-// PV(t) = P(t) V(t) accumulated into O.  The S of tile t+2 is computed while
-// the softmax warps work on tile t+1.
+// item): S_0(0) S_1(0) | PV_0(0) S_0(1) PV_1(0) S_1(1) | PV_0(1) S_0(2) ...
+// S_m(t+1) overwrites the TMEM columns holding P_m(t); it is issued after the
+// PV that reads them, and tcgen05.mma operations from one thread execute in
+// issue order.  Its commit therefore also tells the softmax warps that O_m
+// holds every PV before it (needed before they rescale O_m).
 template <int HD>
 __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
   using C = Cfg<HD>;
-  // Phase parities kept as bits so that no counter array needs memory:
-  // bit m of q_par/p_par/o_par for M-tile m; bit 2m+b of s_par/s_used for
-  // S buffer b of M-tile m.
-  uint32_t ri = 0, u = 0, q_par = 0, p_par = 0, o_par = 0, s_par = 0, s_used = 0;
+  // phase parities as bits (bit m for M-tile m), so no counter needs memory
+  uint32_t ri = 0, u = 0, q_par = 0, p_par = 0, o_par = 0;
   bool ok = true;
   while (ok) {
     const Rec* r = ring_get1(c, p, ri);
@@ -732,40 +762,31 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
     if (!ok) break;
     const uint32_t ub = u;
     u += 2u * (uint32_t)n_t;
-
-    // S(t) for every active M-tile
-    auto issue_s = [&](int t) -> bool {
-      if (!ring_get1(c, p, ri)) return false;  // tile record t (content not needed here)
-      ring_release1(c, ri);
-      ++ri;
-      const uint32_t uk = ub + 2u * (uint32_t)t;
-      const uint32_t ks = uk % C::kStages;
-      if (!wait_bar(c, p, &c.bar.kv_full[ks], (uk / C::kStages) & 1)) return false;
-      const int sb = t & 1;
+    // tile 0: S for every active M-tile
+    if (!ring_get1(c, p, ri)) break;
+    ring_release1(c, ri);
+    ++ri;
+    uint32_t ks = ub % C::kStages;
+    if (!wait_bar(c, p, &c.bar.kv_full[ks], (ub / C::kStages) & 1)) break;
+    tc_fence_after();
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        if (m >= n_m) break;
-        const int bi = 2 * m + sb;
-        if (((s_used >> bi) & 1) &&
-            !wait_bar(c, p, &c.bar.s_free[bi], ((s_par >> bi) & 1) ^ 1))
-          return false;
-        tc_fence_after();
-        issue_qk<HD>(c, m, sb, ks);
-        umma_commit(&c.bar.s_full[bi]);
-        s_par ^= 1u << bi;
-        s_used |= 1u << bi;
-        if (t == n_t - 1) umma_commit(&c.bar.q_empty[m]);  // last read of Q
-      }
-      umma_commit(&c.bar.kv_empty[ks]);
-      return true;
-    };
-
-    ok = issue_s(0);
-    if (ok && n_t > 1) ok = issue_s(1);
+    for (int m = 0; m < 2; ++m) {
+      if (m >= n_m) break;
+      issue_qk<HD>(c, m, ks);
+      umma_commit(&c.bar.s_full[m]);
+      if (n_t == 1) umma_commit(&c.bar.q_empty[m]);
+    }
+    umma_commit(&c.bar.kv_empty[ks]);
     for (int j = 0; j < n_t && ok; ++j) {
       const uint32_t uv = ub + 2u * (uint32_t)j + 1u;
       const uint32_t vs = uv % C::kStages;
       if (!(ok = wait_bar(c, p, &c.bar.kv_full[vs], (uv / C::kStages) & 1))) break;
+      const bool nxt = j + 1 < n_t;
+      if (nxt) {
+        if (!(ok = ring_get1(c, p, ri) != nullptr)) break;
+        ring_release1(c, ri);
+        ++ri;
+      }
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         if (m >= n_m || !ok) break;
@@ -774,15 +795,24 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
         if (j == 0 && !(ok = wait_bar(c, p, &c.bar.o_empty[m], ((o_par >> m) & 1) ^ 1))) break;
         tc_fence_after();
         issue_pv<HD>(c, m, vs, j > 0);
-        umma_commit(&c.bar.pv_done[m]);
-        if (j == n_t - 1) {
+        if (nxt) {
+          if (m == 0) {
+            const uint32_t uk = uv + 1u;
+            ks = uk % C::kStages;
+            if (!(ok = wait_bar(c, p, &c.bar.kv_full[ks], (uk / C::kStages) & 1))) break;
+            tc_fence_after();
+          }
+          issue_qk<HD>(c, m, ks);
+          umma_commit(&c.bar.s_full[m]);
+          if (j + 2 == n_t) umma_commit(&c.bar.q_empty[m]);  // last read of Q
+        } else {
           umma_commit(&c.bar.o_full[m]);
           o_par ^= 1u << m;
         }
       }
       if (!ok) break;
       umma_commit(&c.bar.kv_empty[vs]);
-      if (j + 2 < n_t) ok = issue_s(j + 2);
+      if (nxt) umma_commit(&c.bar.kv_empty[ks]);
     }
   }
   // teardown: wait until every MMA issued by this thread has completed
@@ -794,16 +824,15 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
 // softmax / epilogue (warps 4..11)
 // ============================================================================
 template <int HD>
-__device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq, int lane) {
+__device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq,
+                                            int lane) {
   using C = Cfg<HD>;
   const int r = 32 * wq + lane;  // row within the M-tile == TMEM lane
   const uint32_t lane_addr = static_cast<uint32_t>(32 * wq) << 16;
+  const uint32_t t_s = c.tmem + lane_addr + C::kColS + m * kTileKeys;  // S, then P
   const uint32_t t_o = c.tmem + lane_addr + C::kColO + m * HD;
-  const uint32_t p_row = smem_u32(c.smem + C::kOffP + m * C::kPBytes) + r * 128;
-  const uint32_t sw = r & 7;
   const float sl2 = p.scale_log2;
-  uint32_t ri = 0, on = 0, pvn = 0;
-  uint32_t s_par = 0;  // bit b: parity of the S phases consumed from buffer b
+  uint32_t ri = 0, s_par = 0, o_par = 0;
   while (true) {
     const Rec* rec = ring_get(c, p, ri);
     if (!rec) return;
@@ -829,50 +858,38 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
       if (!t) return;
       const int full = t->w[T_FULL], nvalid = t->w[T_NVALID], kmode = t->w[T_KMODE];
       const int kbase = t->w[T_KBASE];
-      int koff[4];
+      int koff[kChunksPerTile];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) koff[i] = t->w[T_KOFF + i];
+      for (int i = 0; i < kChunksPerTile; ++i) koff[i] = t->w[T_KOFF + i];
       ring_release(c, ri, lane);
       ++ri;
       if (!active) continue;
-      const int sb = j & 1;
-      if (!wait_bar_warp(c, p, &c.bar.s_full[2 * m + sb], (s_par >> sb) & 1)) return;
-      s_par ^= 1u << sb;
+      if (!wait_bar_warp(c, p, &c.bar.s_full[m], s_par & 1)) return;
+      s_par ^= 1u;
       tc_fence_after();
-      uint32_t s0[32], s1[32];
-      tmem_ld64_sync(c.tmem + lane_addr + C::kColS + (2 * m + sb) * kTileKeys, s0, s1);
-      // the S buffer may now be overwritten by the S of tile j+2
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.bar.s_free[2 * m + sb]);
-      float x[64];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        x[k] = __uint_as_float(s0[k]);
-        x[k + 32] = __uint_as_float(s1[k]);
-      }
+      uint32_t sv[kTileKeys];
+      tmem_ld128_sync(t_s, sv);
       if (!full) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
+        for (int k = 0; k < kTileKeys; ++k) {
           int kp = INT_MAX;
           if (k < nvalid) {
             if (kmode == 0) kp = kbase + k;
             else if (kmode == 1) kp = __ldg(p.kv_pos + koff[k >> 4] + (k & 15));
             else kp = __ldg(p.live_pos + kbase + k);
           }
-          if (!(kp < lim)) x[k] = -INFINITY;
+          if (!(kp < lim)) sv[k] = __float_as_uint(-INFINITY);
         }
       }
       // row maximum of the raw scores (the scale is positive), in log2 units
-      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+      float mx[4] = {__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]),
+                     __uint_as_float(sv[3])};
 #pragma unroll
-      for (int k = 4; k < 64; k += 4) {
-        mx0 = fmaxf(mx0, x[k]);
-        mx1 = fmaxf(mx1, x[k + 1]);
-        mx2 = fmaxf(mx2, x[k + 2]);
-        mx3 = fmaxf(mx3, x[k + 3]);
+      for (int k = 4; k < kTileKeys; k += 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(sv[k + i]));
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       const float m_new = fmaxf(m_run, mt);
       bool rescale = false;
       float alpha = 1.0f;
@@ -884,47 +901,41 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
         alpha = ex2_approx(m_run - m_new);
         m_run = m_new;
       }
-      const float ref = m_run == -INFINITY ? 0.f : m_run;
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t w[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = ex2_approx(fmaf(x[2 * k], sl2, -ref));
-        const float p1 = ex2_approx(fmaf(x[2 * k + 1], sl2, -ref));
-        sum0 += p0;
-        sum1 += p1;
-        w[k] = pack_bf16x2(p0, p1);
-      }
-      l_run = l_run * alpha + (sum0 + sum1);
-      if (j > 0) {
-        // P buffer and O are still in use by the PV of tile j-1 until it completes
-        if (!wait_bar_warp(c, p, &c.bar.pv_done[m], (pvn - 1) & 1)) return;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O_m holds all earlier PV products (the S commit came after them)
 #pragma unroll 1
-          for (int c0 = 0; c0 < HD; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32_sync(t_o + c0, o);
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32_sync(t_o + c0, o);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(t_o + c0, o);
-          }
-          tmem_st_wait();
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(t_o + c0, o);
         }
       }
+      const float ref = m_run == -INFINITY ? 0.f : m_run;
+      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        st_shared_v4(p_row + ((cc ^ sw) << 4), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2],
-                     w[4 * cc + 3]);
-      fence_proxy_async_smem();
+      for (int cq = 0; cq < kTileKeys / 32; ++cq) {
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[32 * cq + 2 * k]), sl2, -ref));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[32 * cq + 2 * k + 1]), sl2, -ref));
+          sum0 += p0;
+          sum1 += p1;
+          w[k] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(t_s + 16 * cq, w);  // P over the first 64 S columns
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.bar.p_full[m]);
-      ++pvn;
     }
     if (!active) continue;
-    if (!wait_bar_warp(c, p, &c.bar.o_full[m], on & 1)) return;
-    ++on;
+    if (!wait_bar_warp(c, p, &c.bar.o_full[m], o_par & 1)) return;
+    o_par ^= 1u;
     tc_fence_after();
     if (split < 0) {
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
@@ -1000,10 +1011,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.bar.q_full = c.bar.kv_empty + C::kStages;
   c.bar.q_empty = c.bar.q_full + 2;
   c.bar.s_full = c.bar.q_empty + 2;
-  c.bar.s_free = c.bar.s_full + 4;
-  c.bar.p_full = c.bar.s_free + 4;
-  c.bar.pv_done = c.bar.p_full + 2;
-  c.bar.o_full = c.bar.pv_done + 2;
+  c.bar.p_full = c.bar.s_full + 2;
+  c.bar.o_full = c.bar.p_full + 2;
   c.bar.o_empty = c.bar.o_full + 2;
   c.bar.drain = c.bar.o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -1021,14 +1030,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 0; m < 2; ++m) {
       mbar_init(&c.bar.q_full[m], 1);
       mbar_init(&c.bar.q_empty[m], 1);
+      mbar_init(&c.bar.s_full[m], 1);
       mbar_init(&c.bar.p_full[m], 4);
-      mbar_init(&c.bar.pv_done[m], 1);
       mbar_init(&c.bar.o_full[m], 1);
       mbar_init(&c.bar.o_empty[m], 4);
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&c.bar.s_full[2 * m + b], 1);
-        mbar_init(&c.bar.s_free[2 * m + b], 4);
-      }
     }
     mbar_init(c.bar.drain, 1);
     *c.abort_flag = 0;
@@ -1050,15 +1055,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   c.tmem = *tmem_slot;
 
-  if (warp == 3) {
-    Planner pl(p, c, lane);
-    pl.run();
-  } else if (warp == 0) {
-    run_loader<HD>(c, p, &tm_q, &tm_kp, &tm_vp, &tm_kd, &tm_vd, lane);
-  } else if (warp == 1) {
-    if (lane == 0) run_mma<HD>(c, p);
-  } else if (warp >= 4) {
+  // Register split: the control warpgroup (warps 0-3) gives registers to the
+  // two softmax warpgroups for the duration of the roles (each region is
+  // entered and left with its own setmaxnreg), then both return to the launch
+  // allocation for the common teardown.  The host checks the kernel was
+  // compiled with kRegsLaunch registers per thread before launching it.
+  // Deadlock freedom: the softmax increase waits only for the control
+  // decrease (which never blocks); the barrier after the exchange keeps any
+  // control warp from restoring before it; at the end the control increase is
+  // served by the softmax decrease, which never waits on a control warp.
+  if (warp < 4) {
+    regs_dealloc<kRegsControl>();
+    // No warp may start (and then finish and take registers back) before the
+    // softmax warpgroups' increase has been served from the released pool.
+    named_barrier_sync(1, kThreads);
+    if (warp == 3) {
+      Planner pl(p, c, lane);
+      pl.run();
+    } else if (warp == 0) {
+      run_loader<HD>(c, p, &tm_q, &tm_kp, &tm_vp, &tm_kd, &tm_vd, lane);
+    } else if (warp == 1) {
+      if (lane == 0) run_mma<HD>(c, p);
+    }
+    __syncwarp();
+    regs_alloc<kRegsLaunch>();
+  } else {
+    regs_alloc<kRegsSoftmax>();
+    named_barrier_sync(1, kThreads);
     run_softmax<HD>(c, p, (warp - 4) >> 2, warp & 3, lane);
+    __syncwarp();
+    regs_dealloc<kRegsLaunch>();
   }
 
   tc_fence_before();
@@ -1132,6 +1158,12 @@ cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int g
     cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits for registers released by setmaxnreg.dec; the
+    // split must fit what the block is launched with, or the kernel would stall
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attention_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
     configured = true;
   }
   attention_kernel<HD><<<grid, kThreads, C::kSmemAlloc, stream>>>(maps.q, maps.kp, maps.vp,

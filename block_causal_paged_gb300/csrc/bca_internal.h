@@ -8,8 +8,9 @@
 
 namespace bca {
 
-constexpr int kTileKeys = 64;     // keys per KV tile
+constexpr int kTileKeys = 128;    // keys per KV tile
 constexpr int kChunkKeys = 16;    // keys per TMA box (a page holds whole chunks)
+constexpr int kChunksPerTile = kTileKeys / kChunkKeys;
 constexpr int kRowsPerMTile = 128;
 constexpr int kThreads = 384;     // 12 warps, see the role map in attention.cu
 // Per internal wait: about 2 s at the maximum SM clock (longer when clocked down).

@@ -144,5 +144,7 @@ def test_tile_counters_decode(cuda_lib):
     r = DecodeRun(case)
     r.run()
     full, partial, skipped = bca.read_tile_counters(r.ws)
-    # per KV head: ceil(P/64) prefix tiles + 1 own-block tile, all fully visible
-    assert (full, partial, skipped) == (8 * ((10 + 1) + (1 + 1) + (0 + 1)), 0, 0)
+    # tiles of 128 keys per KV head: 640 prefix keys = 5 full tiles; 64 prefix
+    # keys = 1 tile with 64 valid keys; each 64-key own block = 1 tile with 64
+    # valid keys (masked past the end); nothing is skipped in a decode step
+    assert (full, partial, skipped) == (8 * 5, 8 * (1 + 1 + 1 + 1), 0)

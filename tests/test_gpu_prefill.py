@@ -54,7 +54,7 @@ def test_prefill_4x8192_sampled_rows_and_tile_counts(cuda_lib):
         assert_close(out[cu[b] + rows], ref[cu[b] + rows], what=f"seq {b}")
     full, partial, skipped = bca.read_tile_counters(r.ws)
     pos = np.arange(8192)
-    cls = oracle.tile_classes(pos, pos, 0, 64, 128, 64)   # 128-query x 64-key tiles
+    cls = oracle.tile_classes(pos, pos, 0, 64, 128, 128)  # 128-query x 128-key tiles
     per = 4 * 8 * 2                                        # sequences x kv heads x head pairs
     assert full == per * int((cls == "F").sum())
     assert partial == per * int((cls == "P").sum())
