@@ -634,23 +634,20 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
     const int my_coord = __shfl_sync(0xffffffffu, lane < kChunksPerTile ? coord_of(f, lane) : 0,
                                      my_chunk);
     const bool my_tma = box_lane && (my_nv == 0 || my_nv == kChunkKeys);
+    const int ragged = (nvalid % kChunkKeys) != 0 ? nvalid / kChunkKeys : -1;
     for (int kv = 0; kv < 2 && ok; ++kv) {
       const uint32_t slot = u % C::kStages;
       if (!wait_bar_warp(c, p, &c.bar.kv_empty[slot], ((u / C::kStages) & 1) ^ 1)) { ok = false; break; }
       const uint32_t dst = kv_base + slot * C::kSlotBytes;
-      uint32_t tma_bytes = 0;
-      bool manual = false;
-#pragma unroll
-      for (int i = 0; i < kChunksPerTile; ++i) {
-        const int nv = min(max(nvalid - i * kChunkKeys, 0), kChunkKeys);
-        if (nv == 0 || nv == kChunkKeys) {
-          tma_bytes += C::kHalves * 2048;
-          continue;
-        }
+      // every chunk is full or empty (one box per half, empty ones read out of
+      // range as zeros) except at most the chunk holding the last valid key
+      const bool manual = ragged >= 0;
+      const uint32_t tma_bytes = (uint32_t)(kChunksPerTile - (manual ? 1 : 0)) * C::kHalves * 2048;
+      if (manual) {
         // ragged chunk: copy the valid rows with the warp, zero the rest
-        manual = true;
+        const int nv = nvalid - ragged * kChunkKeys;
         const uint16_t* base = src == 0 ? (kv ? p.v_pool : p.k_pool) : (kv ? p.v_dense : p.k_dense);
-        const int coord = f[T_COORD + i];
+        const int coord = __shfl_sync(0xffffffffu, my_coord, ragged * C::kHalves);
         for (int piece = lane; piece < kChunkKeys * C::kHalves * 8; piece += 32) {
           const int rr = piece / (C::kHalves * 8);
           const int h = (piece / 8) % C::kHalves;
@@ -661,7 +658,7 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
                                         : (size_t)(coord + rr) * p.Hkv + head;
             v = __ldg(reinterpret_cast<const uint4*>(base + row * HD + h * 64 + cc * 8));
           }
-          const int krow = i * kChunkKeys + rr;
+          const int krow = ragged * kChunkKeys + rr;
           st_shared_v4(dst + h * C::kHalfBytes + krow * 128 + ((cc ^ (krow & 7)) << 4), v.x, v.y,
                        v.z, v.w);
         }

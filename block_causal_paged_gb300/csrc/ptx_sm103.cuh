@@ -51,14 +51,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of the given parity to complete, for at most
-// `timeout_cycles` SM clock cycles.  The clock is read only after 1024 failed
+// `timeout_cycles` SM clock cycles (mbar_wait below).  The clock is read only after 1024 failed
 // polls, so a wait that succeeds quickly costs nothing but the polls; the
 // shared abort flag is checked at the same cadence so that one role giving
 // up releases all the others.  Returns false on timeout or abort; the caller
 // then skips to its teardown.
+// Non-blocking test of the phase (returns at once either way).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           long long timeout_cycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // a phase that has already completed is seen by the cheap test; only a real
+  // wait goes through the suspending try_wait loop
+  if (mbar_test_wait(bar, parity)) return true;
   long long t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
