@@ -623,31 +623,39 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
       }
       continue;
     }
-    // a KV tile: K then V, each into the next stage.  Lane l < 8 * halves
-    // copies one 16-key half-row box (chunk l / halves, half l % halves), so a
-    // tile's boxes go out as one warp instruction instead of one per box.
+    // a KV tile: K into the next stage, V into the one after.  Both stages are
+    // acquired first; then one warp instruction issues every box of the tile:
+    // lanes 0-15 the K boxes, lanes 16-31 the V boxes (lane l % 16 < 8 * halves
+    // copies chunk (l % 16) / halves, half (l % 16) % halves).
     const int src = f[T_SRC], nvalid = f[T_NVALID], head = f[T_HEAD];
-    const bool box_lane = lane < kChunksPerTile * C::kHalves;
-    const int my_chunk = box_lane ? lane / C::kHalves : 0;
-    const int my_half = lane % C::kHalves;
+    const int sub = lane & 15;
+    const int my_kv = lane >> 4;                        // 0: K, 1: V
+    const bool box_lane = sub < kChunksPerTile * C::kHalves;
+    const int my_chunk = box_lane ? sub / C::kHalves : 0;
+    const int my_half = sub % C::kHalves;
     const int my_nv = min(max(nvalid - my_chunk * kChunkKeys, 0), kChunkKeys);
     const int my_coord = __shfl_sync(0xffffffffu, lane < kChunksPerTile ? coord_of(f, lane) : 0,
                                      my_chunk);
     const bool my_tma = box_lane && (my_nv == 0 || my_nv == kChunkKeys);
     const int ragged = (nvalid % kChunkKeys) != 0 ? nvalid / kChunkKeys : -1;
-    for (int kv = 0; kv < 2 && ok; ++kv) {
-      const uint32_t slot = u % C::kStages;
-      if (!wait_bar_warp(c, p, &c.bar.kv_empty[slot], ((u / C::kStages) & 1) ^ 1)) { ok = false; break; }
-      const uint32_t dst = kv_base + slot * C::kSlotBytes;
-      // every chunk is full or empty (one box per half, empty ones read out of
-      // range as zeros) except at most the chunk holding the last valid key
-      const bool manual = ragged >= 0;
-      const uint32_t tma_bytes = (uint32_t)(kChunksPerTile - (manual ? 1 : 0)) * C::kHalves * 2048;
-      if (manual) {
-        // ragged chunk: copy the valid rows with the warp, zero the rest
-        const int nv = nvalid - ragged * kChunkKeys;
+    const bool manual = ragged >= 0;
+    const uint32_t tma_bytes = (uint32_t)(kChunksPerTile - (manual ? 1 : 0)) * C::kHalves * 2048;
+    uint32_t slot[2];
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      slot[kv] = (u + kv) % C::kStages;
+      if (ok && !wait_bar_warp(c, p, &c.bar.kv_empty[slot[kv]], (((u + kv) / C::kStages) & 1) ^ 1))
+        ok = false;
+    }
+    if (!ok) break;
+    if (manual) {
+      // ragged chunk: copy the valid rows with the warp, zero the rest
+      const int nv = nvalid - ragged * kChunkKeys;
+      const int coord = __shfl_sync(0xffffffffu, my_coord, ragged * C::kHalves);
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint32_t dst = kv_base + slot[kv] * C::kSlotBytes;
         const uint16_t* base = src == 0 ? (kv ? p.v_pool : p.k_pool) : (kv ? p.v_dense : p.k_dense);
-        const int coord = __shfl_sync(0xffffffffu, my_coord, ragged * C::kHalves);
         for (int piece = lane; piece < kChunkKeys * C::kHalves * 8; piece += 32) {
           const int rr = piece / (C::kHalves * 8);
           const int h = (piece / 8) % C::kHalves;
@@ -663,23 +671,24 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
                        v.z, v.w);
         }
       }
-      if (manual) fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        if (tma_bytes) mbar_arrive_expect_tx(&c.bar.kv_full[slot], tma_bytes);
-        else mbar_arrive(&c.bar.kv_full[slot]);
-      }
-      __syncwarp();
-      if (my_tma) {
-        // the planner made the coordinate out of range for a chunk with no key
-        const CUtensorMap* map = src == 0 ? (kv ? tm_vp : tm_kp) : (kv ? tm_vd : tm_kd);
-        const uint32_t d = dst + my_half * C::kHalfBytes + my_chunk * 2048;
-        if (src == 0) tma_load_2d(d, map, &c.bar.kv_full[slot], my_half * 64, my_coord);
-        else tma_load_3d(d, map, &c.bar.kv_full[slot], my_half * 64, head, my_coord);
-      }
-      __syncwarp();
-      ++u;
+      fence_proxy_async_smem();
     }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&c.bar.kv_full[slot[0]], tma_bytes);
+      mbar_arrive_expect_tx(&c.bar.kv_full[slot[1]], tma_bytes);
+    }
+    __syncwarp();
+    if (my_tma) {
+      // the planner made the coordinate out of range for a chunk with no key
+      const CUtensorMap* map = src == 0 ? (my_kv ? tm_vp : tm_kp) : (my_kv ? tm_vd : tm_kd);
+      const uint32_t sl = my_kv ? slot[1] : slot[0];
+      const uint32_t d = kv_base + sl * C::kSlotBytes + my_half * C::kHalfBytes + my_chunk * 2048;
+      if (src == 0) tma_load_2d(d, map, &c.bar.kv_full[sl], my_half * 64, my_coord);
+      else tma_load_3d(d, map, &c.bar.kv_full[sl], my_half * 64, head, my_coord);
+    }
+    __syncwarp();
+    u += 2;
   }
   // teardown: never leave this CTA with copies in flight
   for (uint32_t k = 0; k < (uint32_t)C::kStages && k < u; ++k) {
