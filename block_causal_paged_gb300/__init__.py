@@ -69,6 +69,8 @@ SIGNATURES = {
                          _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp], ctypes.c_int),
     "bca_validate_page_table": ([_DP, _vp, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)],
                                 ctypes.c_int),
+    "bca_decode_static_scratch": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                   _vp, _vp], ctypes.c_int),
     "bca_profile_start": ([_i32], ctypes.c_int),
     "bca_profile_stop": ([ctypes.POINTER(KernelTimes)], ctypes.c_int),
 }
@@ -169,6 +171,19 @@ def bca_decode(d: Dims, q, k_blk, v_blk, k_pool, v_pool, page_table, prefix_len,
                            _ptr(v_pool), _ptr(page_table), _ptr(prefix_len), _ptr(out),
                            1 if commit else 0, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "bca_decode")
+
+
+def bca_decode_static_scratch(d: Dims, q, k_blk, v_blk, k_pool, v_pool, page_table, prefix_len,
+                              out, commit: bool, device_status=None, stream=None) -> None:
+    """bca_decode with the library's own fixed scratch array (no workspace).
+
+    For callers that cannot allocate device memory on this path; see
+    include/bca.h for the size limit and the sharing rules."""
+    rc = load().bca_decode_static_scratch(ctypes.byref(d), _ptr(q), _ptr(k_blk), _ptr(v_blk),
+                                          _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+                                          _ptr(prefix_len), _ptr(out), 1 if commit else 0,
+                                          _ptr(device_status), _stream(stream))
+    _check(rc, "bca_decode_static_scratch")
 
 
 def bca_commit_kv(d: Dims, k_blk, v_blk, k_pool, v_pool, page_table, start_pos, num_tokens: int,

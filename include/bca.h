@@ -239,6 +239,37 @@ int bca_validate_page_table(const bca_dims* dims, const int32_t* page_table_host
                             int32_t* bad_entry);
 
 /*
+ * bca_decode_static_scratch -- bca_decode for callers that cannot allocate.
+ *
+ * The pages describe no counterpart to this call; it is a library-side
+ * convenience.  It computes exactly what bca_decode computes (same inputs,
+ * outputs and commit), but takes no workspace: its scratch is a fixed 16 MiB
+ * device array inside the library, present on every GPU that loads the
+ * library until the process exits.  It is meant for callers that must not
+ * call cudaMalloc on this path: a plugin inside an engine that owns all
+ * device memory and offers it no allocator, a serving loop in which an
+ * allocation (which can synchronize the device or fail under fragmentation)
+ * is not acceptable, or a runtime with no access to the CUDA allocator.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *  - A request whose minimum decode scratch exceeds the array
+ *    (bca_workspace_size(dims, BCA_OP_DECODE_MIN) > 16 MiB) is rejected with
+ *    BCA_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents:
+ *    the status header is cleared at the start of each call, and calls that
+ *    overlap on the GPU (other streams, other host threads) race on it.
+ *  - device_status: optional device int32 that receives, in stream order, the
+ *    first device-detected error of this call (0 if none).
+ */
+int bca_decode_static_scratch(const bca_dims* dims, const void* q, const void* k_blk,
+                              const void* v_blk, void* k_pool, void* v_pool,
+                              const int32_t* page_table, const int32_t* prefix_len, void* out,
+                              int commit, int32_t* device_status, bca_stream_t stream);
+
+/*
  * Kernel timing for benchmarks (not on any computation path).  While a
  * profile is active, every entry point records a CUDA event pair around each
  * kernel it launches, on the call's own stream; bca_profile_stop synchronizes
