@@ -246,6 +246,27 @@ def workload_config(args, prefix_len):
 # our arm
 # ---------------------------------------------------------------------------
 
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank serves its own batch (weak scaling): a distinct seeded workload."""
+    return base_seed + rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Slowest rank's value (the job's step time); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time."""
+    return flops_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def time_steps(torch, fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -281,7 +302,7 @@ def run_ours(args):
 
     def build_case(D):
         # each rank runs its own batch (weak scaling): seed offset by rank
-        case = workloads.serving_decode(seed=args.seed + rank, D=D, B=args.batch,
+        case = workloads.serving_decode(seed=rank_seed(args.seed, rank), D=D, B=args.batch,
                                         keep_logical=False)
         S = case.pool.page_size
         dd = bca.dims(case.B, D, case.Hq, case.Hkv, case.d, S, case.pool.num_pages,
@@ -331,12 +352,8 @@ def run_ours(args):
         return case, dd, t, ms / steps, clocks, prof, alg
 
     case, dd, t, ms_step, clocks, prof, alg = measure(args.D, args.steps, args.warmup, True)
-    ms_all = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_all, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_all.item())
-    flops_total = alg["flops"] * world  # every rank runs the same-shaped workload
-    value = flops_total / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms_step, dev)
+    value = job_throughput_tflops(alg["flops"], world, ms_max)
 
     traffic, traffic_src = committed_traffic(args.batch, args.D)
     if args.traffic is not None:
@@ -386,10 +403,8 @@ def run_ours(args):
     e2e_steps = max(10, args.steps // 4)
     barrier()
     e2e_ms = time_steps(torch, e2e_step, e2e_steps, stream) / e2e_steps
-    e_all = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e_all, op=dist.ReduceOp.MAX)
-    e2e_value = flops_total / (float(e_all.item()) * 1e-3) / 1e12
+    e2e_ms_max = max_over_ranks(e2e_ms, dev)
+    e2e_value = job_throughput_tflops(alg["flops"], world, e2e_ms_max)
     st = bca.read_device_status(t["ws"])
     del t, case
 
@@ -422,7 +437,7 @@ def run_ours(args):
                 "hbm_gbs": alg["step_bytes"] / (ms_max * 1e-3) / 1e9,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": d2h, "ms_per_step": float(e_all.item())},
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
                 "gpu_launches": int(round(launches_per_step * args.steps)),
                 "launches_per_step": launches_per_step,
                 "kernel_ms": {k: (v[1] / v[0] if v[0] else None) for k, v in prof.items()},
