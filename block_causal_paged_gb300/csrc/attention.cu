@@ -593,18 +593,24 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
   // phase bits (bit m): Q loads issued per M-tile (parity) and whether any
   uint32_t ri = 0, u = 0, q_par = 0, q_used = 0;
   bool ok = true;
+  const bool box_lane = (lane & 15) < kChunksPerTile * C::kHalves;
+  const int my_chunk = box_lane ? (lane & 15) / C::kHalves : 0;
+  const int my_half = (lane & 15) % C::kHalves;
+  const int my_kv = lane >> 4;  // lanes 0-15 copy K boxes, lanes 16-31 V boxes
   while (ok) {
     const Rec* r = ring_get(c, p, ri);
     if (!r) break;
     const int kind = r->w[0];
-    int f[24];
-#pragma unroll
-    for (int i = 0; i < 24; ++i) f[i] = r->w[i];
-    ring_release(c, ri, lane);
-    ++ri;
-    if (kind == kRecEnd) break;
+    if (kind == kRecEnd) {
+      ring_release(c, ri, lane);
+      break;
+    }
     if (kind == kRecItem) {
-      const int n_m = f[I_NM];
+      const int n_m = r->w[I_NM];
+      const int qh0 = r->w[I_QHEAD], qh1 = r->w[I_QHEAD + 1];
+      const int qt0 = r->w[I_QTOK], qt1 = r->w[I_QTOK + 1];
+      ring_release(c, ri, lane);
+      ++ri;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         if (m >= n_m) break;
@@ -615,7 +621,7 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h)
             tma_load_3d(q_base + m * C::kQBytes + h * 16384, tm_q, &c.bar.q_full[m], h * 64,
-                        f[I_QHEAD + m], f[I_QTOK + m]);
+                        m ? qh1 : qh0, m ? qt1 : qt0);
         }
         __syncwarp();
         q_par ^= 1u << m;
@@ -623,21 +629,19 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
       }
       continue;
     }
+    // fields of a tile record: each box lane reads only its own chunk's coordinate
+    const int src = r->w[T_SRC], nvalid = r->w[T_NVALID], head = r->w[T_HEAD];
+    const int my_coord = r->w[T_COORD + my_chunk];
+    const int ragged = (nvalid % kChunkKeys) != 0 ? nvalid / kChunkKeys : -1;
+    const int ragged_coord = ragged >= 0 ? r->w[T_COORD + ragged] : 0;
+    ring_release(c, ri, lane);
+    ++ri;
     // a KV tile: K into the next stage, V into the one after.  Both stages are
     // acquired first; then one warp instruction issues every box of the tile:
     // lanes 0-15 the K boxes, lanes 16-31 the V boxes (lane l % 16 < 8 * halves
     // copies chunk (l % 16) / halves, half (l % 16) % halves).
-    const int src = f[T_SRC], nvalid = f[T_NVALID], head = f[T_HEAD];
-    const int sub = lane & 15;
-    const int my_kv = lane >> 4;                        // 0: K, 1: V
-    const bool box_lane = sub < kChunksPerTile * C::kHalves;
-    const int my_chunk = box_lane ? sub / C::kHalves : 0;
-    const int my_half = sub % C::kHalves;
     const int my_nv = min(max(nvalid - my_chunk * kChunkKeys, 0), kChunkKeys);
-    const int my_coord = __shfl_sync(0xffffffffu, lane < kChunksPerTile ? coord_of(f, lane) : 0,
-                                     my_chunk);
     const bool my_tma = box_lane && (my_nv == 0 || my_nv == kChunkKeys);
-    const int ragged = (nvalid % kChunkKeys) != 0 ? nvalid / kChunkKeys : -1;
     const bool manual = ragged >= 0;
     const uint32_t tma_bytes = (uint32_t)(kChunksPerTile - (manual ? 1 : 0)) * C::kHalves * 2048;
     uint32_t slot[2];
@@ -651,7 +655,7 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, co
     if (manual) {
       // ragged chunk: copy the valid rows with the warp, zero the rest
       const int nv = nvalid - ragged * kChunkKeys;
-      const int coord = __shfl_sync(0xffffffffu, my_coord, ragged * C::kHalves);
+      const int coord = ragged_coord;
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
         const uint32_t dst = kv_base + slot[kv] * C::kSlotBytes;
