@@ -23,7 +23,8 @@
 //   warp 0      loader   : TMA loads of Q and of K/V page boxes into a ring of
 //                          shared-memory stages (ragged 16-key chunks are
 //                          copied by the warp's lanes with zero fill)
-//   warp 1      MMA      : one thread issues tcgen05.mma.  Per M-tile m and
+//   warp 1      MMA      : the whole warp runs the issue loop and one elected
+//                          lane issues each tcgen05.mma.  Per M-tile m and
 //                          tile j: O_m += P_m V_j with P_m read from TMEM, then
 //                          S_m = Q_m K_{j+1}^T into the same TMEM columns; the
 //                          two M-tiles alternate, so the tensor core works on
@@ -562,13 +563,6 @@ __device__ __forceinline__ void ring_release(const Ctx& c, uint32_t i, int lane)
   if (lane == 0) mbar_arrive(&c.bar.rec_empty[i % kNumRec]);
 }
 // Single-thread role (the MMA issuer).
-__device__ __forceinline__ const Rec* ring_get1(const Ctx& c, const AttnParams& p, uint32_t i) {
-  if (!wait_bar(c, p, &c.bar.rec_full[i % kNumRec], (i / kNumRec) & 1)) return nullptr;
-  return &c.ring[i % kNumRec];
-}
-__device__ __forceinline__ void ring_release1(const Ctx& c, uint32_t i) {
-  mbar_arrive(&c.bar.rec_empty[i % kNumRec]);
-}
 
 // ============================================================================
 // loader (warp 0)
@@ -750,22 +744,22 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int m, uint32_t slot, boo
 // issue order.  Its commit therefore also tells the softmax warps that O_m
 // holds every PV before it (needed before they rescale O_m).
 template <int HD>
-__device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
+__device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p, int lane) {
   using C = Cfg<HD>;
   // phase parities as bits (bit m for M-tile m), so no counter needs memory
   uint32_t ri = 0, u = 0, q_par = 0, p_par = 0, o_par = 0;
   bool ok = true;
   while (ok) {
-    const Rec* r = ring_get1(c, p, ri);
+    const Rec* r = ring_get(c, p, ri);
     if (!r) break;
     const int kind = r->w[I_KIND], n_t = r->w[I_NT], n_m = r->w[I_NM];
-    ring_release1(c, ri);
+    ring_release(c, ri, lane);
     ++ri;
     if (kind == kRecEnd) break;
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       if (m < n_m && ok) {
-        ok = wait_bar(c, p, &c.bar.q_full[m], (q_par >> m) & 1);
+        ok = wait_bar_warp(c, p, &c.bar.q_full[m], (q_par >> m) & 1);
         q_par ^= 1u << m;
       }
     }
@@ -773,11 +767,11 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
     const uint32_t ub = u;
     u += 2u * (uint32_t)n_t;
     // tile 0: S for every active M-tile
-    if (!ring_get1(c, p, ri)) break;
-    ring_release1(c, ri);
+    if (!ring_get(c, p, ri)) break;
+    ring_release(c, ri, lane);
     ++ri;
     uint32_t ks = ub % C::kStages;
-    if (!wait_bar(c, p, &c.bar.kv_full[ks], (ub / C::kStages) & 1)) break;
+    if (!wait_bar_warp(c, p, &c.bar.kv_full[ks], (ub / C::kStages) & 1)) break;
     tc_fence_after();
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
@@ -790,26 +784,26 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
     for (int j = 0; j < n_t && ok; ++j) {
       const uint32_t uv = ub + 2u * (uint32_t)j + 1u;
       const uint32_t vs = uv % C::kStages;
-      if (!(ok = wait_bar(c, p, &c.bar.kv_full[vs], (uv / C::kStages) & 1))) break;
+      if (!(ok = wait_bar_warp(c, p, &c.bar.kv_full[vs], (uv / C::kStages) & 1))) break;
       const bool nxt = j + 1 < n_t;
       if (nxt) {
-        if (!(ok = ring_get1(c, p, ri) != nullptr)) break;
-        ring_release1(c, ri);
+        if (!(ok = ring_get(c, p, ri) != nullptr)) break;
+        ring_release(c, ri, lane);
         ++ri;
       }
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         if (m >= n_m || !ok) break;
-        if (!(ok = wait_bar(c, p, &c.bar.p_full[m], (p_par >> m) & 1))) break;
+        if (!(ok = wait_bar_warp(c, p, &c.bar.p_full[m], (p_par >> m) & 1))) break;
         p_par ^= 1u << m;
-        if (j == 0 && !(ok = wait_bar(c, p, &c.bar.o_empty[m], ((o_par >> m) & 1) ^ 1))) break;
+        if (j == 0 && !(ok = wait_bar_warp(c, p, &c.bar.o_empty[m], ((o_par >> m) & 1) ^ 1))) break;
         tc_fence_after();
         issue_pv<HD>(c, m, vs, j > 0);
         if (nxt) {
           if (m == 0) {
             const uint32_t uk = uv + 1u;
             ks = uk % C::kStages;
-            if (!(ok = wait_bar(c, p, &c.bar.kv_full[ks], (uk / C::kStages) & 1))) break;
+            if (!(ok = wait_bar_warp(c, p, &c.bar.kv_full[ks], (uk / C::kStages) & 1))) break;
             tc_fence_after();
           }
           issue_qk<HD>(c, m, ks);
@@ -825,7 +819,7 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p) {
       if (nxt) umma_commit(&c.bar.kv_empty[ks]);
     }
   }
-  // teardown: wait until every MMA issued by this thread has completed
+  // teardown: wait until every MMA issued by this warp has completed
   umma_commit(c.bar.drain);
   mbar_wait(c.bar.drain, 0, c.abort_flag, kWaitTimeoutCycles);
 }
@@ -891,15 +885,17 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
           if (!(kp < lim)) sv[k] = __float_as_uint(-INFINITY);
         }
       }
-      // row maximum of the raw scores (the scale is positive), in log2 units
+      // row maximum of the raw scores (the scale is positive), in log2 units:
+      // four chains of three-input maxima
       float mx[4] = {__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]),
                      __uint_as_float(sv[3])};
 #pragma unroll
-      for (int k = 4; k < kTileKeys; k += 4) {
+      for (int k = 4; k < kTileKeys; k += 8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(sv[k + i]));
+        for (int i = 0; i < 4; ++i)
+          mx[i] = fmax3(mx[i], __uint_as_float(sv[k + 2 * i]), __uint_as_float(sv[k + 2 * i + 1]));
       }
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+      const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
       const float m_new = fmaxf(m_run, mt);
       bool rescale = false;
       float alpha = 1.0f;
@@ -923,21 +919,24 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
         }
       }
       const float ref = m_run == -INFINITY ? 0.f : m_run;
-      float sum0 = 0.f, sum1 = 0.f;
+      // p = 2^(s * scale * log2(e) - ref), two keys per paired FMA / add
+      const float2 scale2 = make_float2(sl2, sl2), nref2 = make_float2(-ref, -ref);
+      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int cq = 0; cq < kTileKeys / 32; ++cq) {
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[32 * cq + 2 * k]), sl2, -ref));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[32 * cq + 2 * k + 1]), sl2, -ref));
-          sum0 += p0;
-          sum1 += p1;
-          w[k] = pack_bf16x2(p0, p1);
+          const float2 x = ffma2(make_float2(__uint_as_float(sv[32 * cq + 2 * k]),
+                                             __uint_as_float(sv[32 * cq + 2 * k + 1])),
+                                 scale2, nref2);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          sum2 = fadd2(sum2, pp);
+          w[k] = pack_bf16x2(pp.x, pp.y);
         }
         tmem_st16(t_s + 16 * cq, w);  // P over the first 64 S columns
       }
-      l_run = l_run * alpha + (sum0 + sum1);
+      l_run = l_run * alpha + (sum2.x + sum2.y);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -1085,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 0) {
       run_loader<HD>(c, p, &tm_q, &tm_kp, &tm_vp, &tm_kd, &tm_vd, lane);
     } else if (warp == 1) {
-      if (lane == 0) run_mma<HD>(c, p);
+      run_mma<HD>(c, p, lane);
     }
     __syncwarp();
     regs_alloc<kRegsLaunch>();
