@@ -213,23 +213,25 @@ DecodeWsLayout decode_ws_layout(int B, int Hkv, int n_rb, int head_dim, int n_sm
   l.split_base_off = kWsHeaderBytes;
   l.items_off = l.split_base_off + round_up((size_t)(B > 0 ? B : 1) * 4, 256);
   l.items_cap = n_sms * kWaves + B * Hkv * n_rb;
-  l.ml_off = l.items_off + round_up((size_t)l.items_cap * 32, 256);
-  l.bytes_per_slot = 256 * 2 * 4 + (size_t)256 * head_dim * 4;
+  l.slot_off = l.items_off + round_up((size_t)l.items_cap * 32, 256);
+  // per split slot: its table entry, (max, sum) for 256 rows, O for 256 rows
+  l.bytes_per_slot = 16 + 256 * 2 * 4 + (size_t)256 * head_dim * 4;
   l.cap = 0;
-  if (ws_bytes > l.ml_off + 256)
-    l.cap = (int)std::min<size_t>((ws_bytes - l.ml_off - 256) / l.bytes_per_slot, 1 << 30);
+  if (ws_bytes > l.slot_off + 512)
+    l.cap = (int)std::min<size_t>((ws_bytes - l.slot_off - 512) / l.bytes_per_slot, 1 << 30);
+  l.ml_off = l.slot_off + round_up((size_t)l.cap * 16, 256);
   l.o_off = l.ml_off + round_up((size_t)l.cap * 256 * 2 * 4, 256);
   return l;
 }
 
 size_t decode_ws_minimum(int B, int Hkv, int n_rb, int head_dim, int n_sms) {
-  return decode_ws_layout(B, Hkv, n_rb, head_dim, n_sms, 0).ml_off;
+  return decode_ws_layout(B, Hkv, n_rb, head_dim, n_sms, 0).slot_off;
 }
 
 size_t decode_ws_recommended(int B, int Hkv, int n_rb, int head_dim, int n_sms) {
   DecodeWsLayout l = decode_ws_layout(B, Hkv, n_rb, head_dim, n_sms, 0);
   // split slots never exceed the work items
-  return l.ml_off + (size_t)l.items_cap * l.bytes_per_slot + 512;
+  return l.slot_off + (size_t)l.items_cap * l.bytes_per_slot + 512;
 }
 
 }  // namespace bca
@@ -368,7 +370,7 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
   const int n_rb0 = ceil_div_i(d->block_size, 2 * (128 / G0));
   const DecodeWsLayout lay =
       decode_ws_layout(d->batch, d->num_kv_heads, n_rb0, d->head_dim, di.sms, ws_bytes);
-  if (ws_bytes < lay.ml_off) return BCA_ERR_WORKSPACE;
+  if (ws_bytes < lay.slot_off) return BCA_ERR_WORKSPACE;
 
   AttnParams p = base_params(d);
   p.mode = kModeDecode;
@@ -388,9 +390,13 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
   p.split_base = (int32_t*)((char*)ws + lay.split_base_off);
   p.items = (int4*)((char*)ws + lay.items_off);
   p.items_cap = lay.items_cap;
+  p.slot_info = (int4*)((char*)ws + lay.slot_off);
   p.part_ml = (float*)((char*)ws + lay.ml_off);
   p.part_o = (float*)((char*)ws + lay.o_off);
   p.split_cap = lay.cap;
+  // the commit of the block runs inside the attention kernel (its warp 2)
+  p.commit_k = commit ? (uint16_t*)k_pool : nullptr;
+  p.commit_v = commit ? (uint16_t*)v_pool : nullptr;
 
   AttnMaps maps;
   const int HD = d->head_dim;
@@ -412,29 +418,8 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
   if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;
   if (max_tiles > kChMin) {
-    if (timed(BCA_KERNEL_COMBINE, s, [&] { return launch_decode_combine(p, HD, s); }) != cudaSuccess)
+    if (timed(BCA_KERNEL_COMBINE, s, [&] { return launch_decode_combine(p, HD, di.sms, s); }) != cudaSuccess)
       return BCA_ERR_CUDA;
-  }
-  if (commit) {
-    CommitParams c;
-    std::memset(&c, 0, sizeof(c));
-    c.k_src = (const uint16_t*)k_blk;
-    c.v_src = (const uint16_t*)v_blk;
-    c.k_pool = (uint16_t*)k_pool;
-    c.v_pool = (uint16_t*)v_pool;
-    c.page_table = page_table;
-    c.start_pos = prefix_len;
-    c.rows_per_seq = d->block_size;
-    c.num_tokens = d->block_size;
-    c.max_rows = d->block_size;
-    c.B = d->batch;
-    c.Hkv = d->num_kv_heads;
-    c.d = HD;
-    c.S = d->page_size;
-    c.num_pages = d->num_pages;
-    c.max_pages = d->max_pages_per_seq;
-    c.hdr = p.hdr;
-    if (timed(BCA_KERNEL_COMMIT, s, [&] { return launch_commit(c, s); }) != cudaSuccess) return BCA_ERR_CUDA;
   }
   return BCA_OK;
 }

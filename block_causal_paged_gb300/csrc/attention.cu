@@ -321,7 +321,7 @@ struct Planner {
   }
 
   // Decode items come from the plan kernel's list, longest sequences first:
-  // {b, g, rb, split slot} {first tile, end tile, prefix length, -}.
+  // {b, g, rb, split slot} {first tile, end tile, prefix length, chunks}.
   __device__ void run_decode() {
     const int n_items = *reinterpret_cast<volatile int*>(&p.hdr->n_items);
     while (ok) {
@@ -825,6 +825,58 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p, int l
 }
 
 // ============================================================================
+// KV commit of a decode block (warp 2, idle after the TMEM allocation): the
+// block's rows P .. P+D-1 are copied from the dense block K/V into their
+// pages.  The attention of this step never reads pool rows at or after P
+// (full 16-key boxes lie below P, ragged ones are copied row by row up to
+// the last valid key), so the copy may run concurrently with it.
+// ============================================================================
+template <int HD>
+__device__ __forceinline__ void run_commit(const AttnParams& p, int lane) {
+  constexpr int kPerHead = HD / 8;  // 16-byte pieces per head row
+  const int D = p.Dblk, Hkv = p.Hkv, per_row = Hkv * kPerHead;
+  const long long rows = (long long)p.B * D;
+  const uint4* kd_src = reinterpret_cast<const uint4*>(p.k_dense);
+  const uint4* vd_src = reinterpret_cast<const uint4*>(p.v_dense);
+  uint4* kd = reinterpret_cast<uint4*>(p.commit_k);
+  uint4* vd = reinterpret_cast<uint4*>(p.commit_v);
+  // 32 rows per pass: lane l resolves the page of row base + l
+  for (long long base = blockIdx.x; base < rows; base += 32ll * gridDim.x) {
+    const long long my_row = base + (long long)lane * gridDim.x;
+    int my_page = -1, my_slot = 0;
+    if (my_row < rows) {
+      const int b = (int)(my_row / D), t = (int)(my_row % D);
+      const int P = __ldg(p.lens + b);
+      if (P >= 0 && P % D == 0 && (long long)P + D <= (long long)p.max_pages * p.S) {
+        const int pos = P + t;
+        const int page = __ldg(p.page_table + (size_t)b * p.max_pages + pos / p.S);
+        if (page >= 0 && page < p.num_pages) {
+          my_page = page;
+          my_slot = pos % p.S;
+        } else {
+          record_error(p, kErrPageOob);
+        }
+      }  // a bad prefix length is reported by the plan kernel
+    }
+    for (int j = 0; j < 32; ++j) {
+      const long long row = base + (long long)j * gridDim.x;
+      if (row >= rows) break;
+      const int page = __shfl_sync(0xffffffffu, my_page, j);
+      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+      if (page < 0) continue;
+      for (int i = lane; i < per_row; i += 32) {
+        const int h = i / kPerHead, cc = i % kPerHead;
+        const size_t dst = (((size_t)page * Hkv + h) * p.S + slot) * kPerHead + cc;
+        const uint4 kv = __ldg(kd_src + row * per_row + i);
+        const uint4 vv = __ldg(vd_src + row * per_row + i);
+        kd[dst] = kv;
+        vd[dst] = vv;
+      }
+    }
+  }
+}
+
+// ============================================================================
 // softmax / epilogue (warps 4..11)
 // ============================================================================
 template <int HD>
@@ -1063,6 +1115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   c.tmem = *tmem_slot;
+  // Programmatic dependent launch: the prologue above overlapped the plan
+  // kernel; nothing it wrote is read before this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // Register split: the control warpgroup (warps 0-3) gives registers to the
   // two softmax warpgroups for the duration of the roles (each region is
@@ -1085,6 +1141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       run_loader<HD>(c, p, &tm_q, &tm_kp, &tm_vp, &tm_kd, &tm_vd, lane);
     } else if (warp == 1) {
       run_mma<HD>(c, p, lane);
+    } else if (p.commit_k != nullptr) {
+      run_commit<HD>(p, lane);
     }
     __syncwarp();
     regs_alloc<kRegsLaunch>();
@@ -1101,60 +1159,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(c.tmem, C::kTmemCols);
-  }
-}
-
-// ============================================================================
-// split-KV combine (decode): O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c
-// ============================================================================
-template <int HD>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p) {
-  const int per_b = p.Hkv * p.n_rb;
-  const int b = blockIdx.x / per_b;
-  const int rem = blockIdx.x % per_b;
-  const int g = rem / p.n_rb, rb = rem % p.n_rb;
-  const int D = p.Dblk;
-  int P = __ldg(p.lens + b);
-  if (P < 0 || P % D != 0 || (long long)P + D > (long long)p.max_pages * p.S) P = 0;
-  const int nt = ceil_div(P, kTileKeys) + ceil_div(D, kTileKeys);
-  const int CH = p.hdr->chunk_tiles;
-  const int nch = ceil_div(nt, CH);
-  if (nch <= 1) return;
-  const int R = threadIdx.x;
-  const int m = R / kRowsPerMTile, r = R % kRowsPerMTile;
-  const int tok = rb * 2 * p.tpm + m * p.tpm + r / p.hpr;
-  if (r >= p.hpr * p.tpm || tok >= D) return;
-  const int base = p.split_base[b] + (g * p.n_rb + rb) * nch;
-  float M = -INFINITY;
-  for (int ci = 0; ci < nch; ++ci) M = fmaxf(M, p.part_ml[((size_t)(base + ci) * 256 + R) * 2]);
-  float acc[HD];
-#pragma unroll
-  for (int k = 0; k < HD; ++k) acc[k] = 0.f;
-  float den = 0.f;
-  for (int ci = 0; ci < nch; ++ci) {
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((size_t)(base + ci) * 256 + R) * 2);
-    const float w = ml.x == -INFINITY ? 0.f : ex2_approx(ml.x - M);
-    den += w * ml.y;
-#pragma unroll
-    for (int k4 = 0; k4 < HD / 4; ++k4) {
-      const float4 v = *reinterpret_cast<const float4*>(
-          p.part_o + (((size_t)(base + ci) * (HD / 4) + k4) * 256 + R) * 4);
-      acc[4 * k4 + 0] += w * v.x;
-      acc[4 * k4 + 1] += w * v.y;
-      acc[4 * k4 + 2] += w * v.z;
-      acc[4 * k4 + 3] += w * v.w;
-    }
-  }
-  const float inv = den > 0.f ? 1.0f / den : 0.f;
-  uint16_t* dst = p.out + ((size_t)(b * D + tok) * p.Hq + g * p.G + (r % p.hpr)) * HD;
-#pragma unroll
-  for (int k = 0; k < HD; k += 8) {
-    uint4 v;
-    v.x = pack_bf16x2(acc[k + 0] * inv, acc[k + 1] * inv);
-    v.y = pack_bf16x2(acc[k + 2] * inv, acc[k + 3] * inv);
-    v.z = pack_bf16x2(acc[k + 4] * inv, acc[k + 5] * inv);
-    v.w = pack_bf16x2(acc[k + 6] * inv, acc[k + 7] * inv);
-    *reinterpret_cast<uint4*>(dst + k) = v;
   }
 }
 
@@ -1175,9 +1179,18 @@ cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int g
     if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
     configured = true;
   }
-  attention_kernel<HD><<<grid, kThreads, C::kSmemAlloc, stream>>>(maps.q, maps.kp, maps.vp,
-                                                                  maps.kd, maps.vd, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attention_kernel<HD>, maps.q, maps.kp, maps.vp, maps.kd,
+                            maps.vd, p);
 }
 
 }  // namespace
@@ -1186,14 +1199,6 @@ cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head
                              cudaStream_t stream) {
   if (head_dim == 128) return launch_attention_hd<128>(p, maps, grid, stream);
   return launch_attention_hd<64>(p, maps, grid, stream);
-}
-
-cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, cudaStream_t stream) {
-  const int blocks = p.B * p.Hkv * p.n_rb;
-  if (blocks == 0) return cudaSuccess;
-  if (head_dim == 128) combine_kernel<128><<<blocks, 256, 0, stream>>>(p);
-  else combine_kernel<64><<<blocks, 256, 0, stream>>>(p);
-  return cudaGetLastError();
 }
 
 }  // namespace bca

@@ -27,17 +27,19 @@ struct WsHeader {
   unsigned long long tiles_full;
   unsigned long long tiles_partial;
   unsigned long long tiles_skipped;
-  int32_t reserved1[54];
+  int32_t n_split_slots;   // decode: split-KV slots in use (plan kernel)
+  int32_t reserved1[53];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 constexpr size_t kWsHeaderBytes = 256;
 
 // Decode workspace: header | split_base int32[B] | item list int4[2][items_cap]
-// | partial (max, sum) float2[cap][256] | partial O float[cap][d/4][256][4]
-// (regions 256-byte aligned).  items_cap bounds the number of work items
-// (n_sms * waves + B * Hkv * n_rb); cap (split-KV slots) is whatever fits.
+// | slot table int4[cap] | partial (max, sum) float2[cap][256] | partial O
+// float[cap][d/4][256][4] (regions 256-byte aligned).  items_cap bounds the
+// number of work items (n_sms * waves + B * Hkv * n_rb); cap (split-KV slots)
+// is whatever fits.
 struct DecodeWsLayout {
-  size_t split_base_off, items_off, ml_off, o_off, bytes_per_slot;
+  size_t split_base_off, items_off, slot_off, ml_off, o_off, bytes_per_slot;
   int items_cap;
   int cap;
 };
@@ -73,9 +75,14 @@ struct AttnParams {
   int32_t* split_base;
   int4* items;               // decode: item list written by the plan kernel
   int items_cap;
+  int4* slot_info;           // decode: per split slot {b, g << 16 | rb, first slot of its group, chunks}
   float* part_ml;
   float* part_o;
   int split_cap;
+  // decode with commit: the block's K/V (k_dense / v_dense) is copied into
+  // these pools by the attention kernel itself (null: no commit)
+  uint16_t* commit_k;
+  uint16_t* commit_v;
 };
 
 struct AttnMaps {
@@ -90,8 +97,9 @@ cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream)
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head_dim, int grid,
                              cudaStream_t stream);
 
-// Split-KV combine for decode (only sequences that were split do work).
-cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, cudaStream_t stream);
+// Split-KV combine for decode: one CTA per (split group, 32 head-dim columns),
+// over the slot table the plan kernel wrote.
+cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, int n_sms, cudaStream_t stream);
 
 // Bit copy of K/V rows into pages.  Source rows are [rows, Hkv, d]; sequence
 // b owns rows src_first(b) .. src_first(b)+count(b)-1 and writes them to

@@ -1,0 +1,113 @@
+// Split-KV combine for decode.
+//
+// A long prefix is split into chunks that different CTAs attend to (each
+// chunk is an online softmax over its keys, "Paged Attention"), so every row
+// of a split group has, per chunk c, a running maximum m_c (log2 units), a sum
+// l_c and an unnormalised output O_c.  Merging them is the same rescaling the
+// online softmax does between tiles:
+//     M = max_c m_c,  O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+//
+// Work unit: one split group (its first slot in the slot table) x 32 head-dim
+// columns; 256 threads, one per row (two M-tiles of 128), so every load of a
+// partial is 512 contiguous bytes per warp and all chunks' loads of a unit are
+// in flight together.  Launched with programmatic dependent launch: the grid
+// may start while the attention kernel drains and waits for it to finish.
+#include <cstdint>
+
+#include "bca_internal.h"
+
+namespace bca {
+namespace {
+
+constexpr int kCombineThreads = 256;  // rows of a split group
+constexpr int kCols = 32;             // head-dim columns per work unit
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  constexpr int kQ = HD / kCols;
+  const int n_slots = *reinterpret_cast<volatile int*>(&p.hdr->n_split_slots);
+  const int R = threadIdx.x;
+  const int m = R / kRowsPerMTile, r = R % kRowsPerMTile;
+  const long long units = (long long)n_slots * kQ;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int s = (int)(u / kQ), q = (int)(u % kQ);
+    const int4 info = p.slot_info[s];
+    if (info.z != s) continue;  // only the first slot of a group does its work
+    const int b = info.x, g = info.y >> 16, rb = info.y & 0xffff, nch = info.w;
+    const int tok = rb * 2 * p.tpm + m * p.tpm + r / p.hpr;
+    if (r >= p.hpr * p.tpm || tok >= p.Dblk) continue;
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+    float M = -INFINITY;
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, ml[(size_t)(s + c) * 256 + R].x);
+    float den = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const float2 v = ml[(size_t)(s + c) * 256 + R];
+      den += (v.x == -INFINITY ? 0.f : ex2f(v.x - M)) * v.y;
+    }
+    const float inv = den > 0.f ? 1.0f / den : 0.f;
+    float acc[kCols];
+#pragma unroll
+    for (int k = 0; k < kCols; ++k) acc[k] = 0.f;
+    const float4* po = reinterpret_cast<const float4*>(p.part_o);
+#pragma unroll 2
+    for (int c = 0; c < nch; ++c) {
+      const float mc = ml[(size_t)(s + c) * 256 + R].x;
+      const float w = mc == -INFINITY ? 0.f : ex2f(mc - M);
+      const float4* src = po + ((size_t)(s + c) * (HD / 4) + q * (kCols / 4)) * 256 + R;
+      float4 v[kCols / 4];
+#pragma unroll
+      for (int k4 = 0; k4 < kCols / 4; ++k4) v[k4] = src[(size_t)k4 * 256];
+#pragma unroll
+      for (int k4 = 0; k4 < kCols / 4; ++k4) {
+        acc[4 * k4 + 0] += w * v[k4].x;
+        acc[4 * k4 + 1] += w * v[k4].y;
+        acc[4 * k4 + 2] += w * v[k4].z;
+        acc[4 * k4 + 3] += w * v[k4].w;
+      }
+    }
+    uint16_t* dst = p.out +
+                    ((size_t)(b * p.Dblk + tok) * p.Hq + g * p.G + (r % p.hpr)) * HD + q * kCols;
+#pragma unroll
+    for (int k = 0; k < kCols; k += 8) {
+      uint4 o;
+      o.x = pack2(acc[k + 0] * inv, acc[k + 1] * inv);
+      o.y = pack2(acc[k + 2] * inv, acc[k + 3] * inv);
+      o.z = pack2(acc[k + 4] * inv, acc[k + 5] * inv);
+      o.w = pack2(acc[k + 6] * inv, acc[k + 7] * inv);
+      *reinterpret_cast<uint4*>(dst + k) = o;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, int n_sms,
+                                  cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (n_sms > 0 ? n_sms : 1));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
+}
+
+}  // namespace bca

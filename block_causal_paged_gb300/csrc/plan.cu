@@ -6,10 +6,14 @@
 //   - chooses the chunk size CH (KV tiles per work item) so that there are
 //     about `waves` items per CTA, never fewer than ch_min tiles per chunk,
 //     and the split-KV partials and the item list fit the workspace;
-//   - orders the sequences longest first (bitonic sort in shared memory) so
-//     that the dynamic schedule hands out the largest items first;
-//   - writes the item list {b, g, rb, split slot}{t0, t1, P, -} and, for each
-//     sequence, the first split-KV slot of its chunks (read by the combine).
+//   - orders the sequences longest first (a rank sort in shared memory: each
+//     thread counts the sequences that go before its own) so that the dynamic
+//     schedule hands out the largest items first;
+//   - writes the item list {b, g, rb, split slot}{t0, t1, P, chunks}, for each
+//     sequence the first split-KV slot of its chunks, and for each split slot
+//     {b, g << 16 | rb, first slot of its group, chunks} (read by the combine).
+// The block is sized to the batch (a multiple of 32 threads, at most 1024),
+// so small batches pay for few warps at every barrier.
 #include <cstdint>
 
 #include "bca_internal.h"
@@ -17,7 +21,7 @@
 namespace bca {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;  // upper bound; the launch uses fewer for small batches
 constexpr int kPlanSortMax = 2048;  // larger batches keep their natural order
 constexpr int kErrBadLength = -17;
 constexpr int kErrWorkspace = -4;
@@ -37,75 +41,104 @@ __device__ __forceinline__ int plan_tiles(const AttnParams& p, int P) {
   return cdiv(P, kTileKeys) + cdiv(p.Dblk, kTileKeys);
 }
 
-// Sum over the block (every thread gets the result).
-__device__ long long block_sum(long long v, long long* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Sums of two values over the block (every thread gets both).
+__device__ longlong2 block_sum2(long long a, long long b, longlong2* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
   __syncthreads();
-  if (lane == 0) red[warp] = v;
+  if (lane == 0) red[warp] = make_longlong2(a, b);
   __syncthreads();
-  long long t = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-  __syncthreads();
+  longlong2 t = make_longlong2(0, 0);
+  for (int w = 0; w < nw; ++w) {
+    t.x += red[w].x;
+    t.y += red[w].y;
+  }
   return t;
 }
 
-// Exclusive prefix sum over the block in thread order; *total gets the sum.
-__device__ long long block_excl_scan(long long v, long long* red, long long* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long x = v;
+// Exclusive prefix sums of two values in thread order; *total gets the sums.
+__device__ longlong2 block_scan2(long long a, long long b, longlong2* red, longlong2* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  long long x = a, y = b;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const long long xo = __shfl_up_sync(0xffffffffu, x, o);
+    const long long yo = __shfl_up_sync(0xffffffffu, y, o);
+    if (lane >= o) {
+      x += xo;
+      y += yo;
+    }
   }
   __syncthreads();
-  if (lane == 31) red[warp] = x;
+  if (lane == 31) red[warp] = make_longlong2(x, y);
   __syncthreads();
-  long long before = 0, all = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-    if (w < warp) before += red[w];
-    all += red[w];
+  longlong2 before = make_longlong2(0, 0), all = make_longlong2(0, 0);
+  for (int w = 0; w < nw; ++w) {
+    if (w < warp) {
+      before.x += red[w].x;
+      before.y += red[w].y;
+    }
+    all.x += red[w].x;
+    all.y += red[w].y;
   }
-  __syncthreads();
   *total = all;
-  return before + x - v;
+  return make_longlong2(before.x + x - a, before.y + y - b);
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ AttnParams p,
                                                             int attn_grid) {
-  __shared__ int s_nt[kPlanSortMax];
-  __shared__ int s_ord[kPlanSortMax];
-  __shared__ int s_base[kPlanSortMax + 1];
-  __shared__ long long s_red[32];
+  __shared__ int s_nt[kPlanSortMax];     // KV tiles per sequence
+  __shared__ int s_P[kPlanSortMax];      // prefix length per sequence
+  __shared__ int s_ord[kPlanSortMax];    // schedule position -> sequence
+  __shared__ int s_split[kPlanSortMax];  // first split slot per sequence
+  __shared__ longlong2 s_red[32];
   const int tid = threadIdx.x;
   const int nth = blockDim.x;
+  // Programmatic dependent launch: the attention kernel may start its
+  // prologue now; everything it reads from here is behind its own wait for
+  // this grid.  This grid in turn waits for the work before it in the stream
+  // (which may still be reading the workspace) before touching anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) p.hdr->work_next = 0;
   if (p.mode != kModeDecode) return;
 
   const int B = p.B;
   const int per_seq = p.Hkv * p.n_rb;
-  const bool sorted = B <= kPlanSortMax;
+  const bool small = B <= kPlanSortMax;  // tables fit in shared memory; sort
 
-  // tiles per sequence and in total
-  int bad = 0;
-  long long tot = 0;
+  // 1. prefix lengths and tiles per sequence
+  long long tot = 0, bad = 0;
   for (int b = tid; b < B; b += nth) {
-    const int nt = plan_tiles(p, plan_prefix(p, b, &bad));
-    if (sorted) s_nt[b] = nt;
+    int bb = 0;
+    const int P = plan_prefix(p, b, &bb);
+    const int nt = plan_tiles(p, P);
+    if (small) {
+      s_nt[b] = nt;
+      s_P[b] = P;
+    }
     tot += nt;
+    bad |= bb;
   }
-  tot = block_sum(tot, s_red) * per_seq;
-  if (__syncthreads_or(bad) && tid == 0) atomicCAS(&p.hdr->status, 0, kErrBadLength);
-
+  const longlong2 t1 = block_sum2(tot, bad, s_red);
+  tot = t1.x * per_seq;
+  if (t1.y && tid == 0) atomicCAS(&p.hdr->status, 0, kErrBadLength);
   auto tiles_of = [&](int b) {
-    if (sorted) return s_nt[b];
+    if (small) return s_nt[b];
     int dummy = 0;
     return plan_tiles(p, plan_prefix(p, b, &dummy));
   };
+  auto prefix_of = [&](int b) {
+    if (small) return s_P[b];
+    int dummy = 0;
+    return plan_prefix(p, b, &dummy);
+  };
 
-  // chunk size: ~waves items per CTA, at least ch_min tiles, fits the workspace
+  // 2. chunk size: ~waves items per CTA, at least ch_min tiles, fits the workspace
   const long long target = (long long)attn_grid * (p.waves > 0 ? p.waves : 1);
   long long ch = (tot + target - 1) / target;
   if (ch < p.ch_min) ch = p.ch_min;
@@ -117,113 +150,91 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       ni += nch;
       if (nch > 1) ns += nch;
     }
-    ns = block_sum(ns, s_red) * per_seq;
-    ni = block_sum(ni, s_red) * per_seq;
-    if (ns <= p.split_cap && ni <= p.items_cap) break;
+    const longlong2 t2 = block_sum2(ns, ni, s_red);
+    if (t2.x * per_seq <= p.split_cap && t2.y * per_seq <= p.items_cap) break;
     ch *= 2;
   }
   const int CH = (int)(ch < (1ll << 30) ? ch : (1ll << 30));
 
-  // longest sequences first (ties by index)
-  if (sorted) {
-    int n2 = 1;
-    while (n2 < B) n2 <<= 1;
-    for (int i = tid; i < n2; i += nth) s_ord[i] = i;
-    __syncthreads();
-    for (int k = 2; k <= n2; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = tid; i < n2; i += nth) {
-          const int ixj = i ^ j;
-          if (ixj > i) {
-            const int a = s_ord[i], c = s_ord[ixj];
-            const int ka = a < B ? s_nt[a] : -1, kc = c < B ? s_nt[c] : -1;
-            const bool a_first = ka > kc || (ka == kc && a < c);
-            const bool up = (i & k) == 0;
-            if (up ? !a_first : a_first) {
-              s_ord[i] = c;
-              s_ord[ixj] = a;
-            }
-          }
-        }
-        __syncthreads();
+  // 3. schedule order, longest first (ties by index): rank of each sequence
+  if (small) {
+    for (int i = tid; i < B; i += nth) {
+      const int ki = s_nt[i];
+      int rank = 0;
+      for (int j = 0; j < B; ++j) {
+        const int kj = s_nt[j];
+        rank += (kj > ki) | ((kj == ki) & (j < i));
       }
+      s_ord[rank] = i;
     }
+    __syncthreads();
   }
-  auto seq_at = [&](int i) { return sorted ? s_ord[i] : i; };
+  auto seq_at = [&](int i) { return small ? s_ord[i] : i; };
 
-  // split-KV slots: in natural sequence order, per-thread contiguous segments
+  // 4. split slots (sequence order) and item bases (schedule order), one scan
+  //    over per-thread contiguous segments of positions
   const int seg = (B + nth - 1) / nth;
   const int lo = min(B, tid * seg), hi = min(B, lo + seg);
-  long long local = 0, total = 0;
+  long long ls = 0, li = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int nch = cdiv(tiles_of(i), CH);
+    if (nch > 1) ls += (long long)nch * per_seq;
+    li += (long long)cdiv(tiles_of(seq_at(i)), CH) * per_seq;
+  }
+  longlong2 all;
+  const longlong2 off = block_scan2(ls, li, s_red, &all);
+  long long so = off.x;
   for (int b = lo; b < hi; ++b) {
+    if (small) s_split[b] = (int)so;
+    p.split_base[b] = (int)so;
     const int nch = cdiv(tiles_of(b), CH);
-    if (nch > 1) local += (long long)nch * per_seq;
+    if (nch > 1) so += (long long)nch * per_seq;
   }
-  long long off = block_excl_scan(local, s_red, &total);
-  for (int b = lo; b < hi; ++b) {
-    p.split_base[b] = (int)off;
-    const int nch = cdiv(tiles_of(b), CH);
-    if (nch > 1) off += (long long)nch * per_seq;
-  }
-  if (total > p.split_cap && tid == 0) atomicCAS(&p.hdr->status, 0, kErrWorkspace);
+  const int n_items = (int)(all.y < p.items_cap ? all.y : p.items_cap);
+  __syncthreads();  // split bases visible to the block
 
-  // item bases in schedule order
-  local = 0;
-  for (int i = lo; i < hi; ++i) local += (long long)cdiv(tiles_of(seq_at(i)), CH) * per_seq;
-  off = block_excl_scan(local, s_red, &total);
-  const int n_items = (int)(total < p.items_cap ? total : p.items_cap);
-  if (sorted) {
-    for (int i = lo; i < hi; ++i) {
-      s_base[i] = (int)off;
-      off += (long long)cdiv(tiles_of(seq_at(i)), CH) * per_seq;
-    }
-    if (tid == 0) s_base[B] = (int)total;
-  }
-  __syncthreads();  // split_base (global) and s_base visible to the block
-
-  auto write_item = [&](int idx, int b, int l) {
-    const int nt = tiles_of(b);
+  // 5. items: each thread writes those of the sequences at its positions
+  long long io = off.y;
+  for (int i = lo; i < hi; ++i) {
+    const int b = seq_at(i);
+    const int nt = tiles_of(b), P = prefix_of(b);
     const int nch = cdiv(nt, CH);
-    const int c = l / per_seq, rest = l % per_seq;
-    const int g = rest / p.n_rb, rb = rest % p.n_rb;
-    const int t0 = c * CH, t1 = min(nt, t0 + CH);
-    const int split = nch > 1 ? p.split_base[b] + (g * p.n_rb + rb) * nch + c : -1;
-    int dummy = 0;
-    const int P = plan_prefix(p, b, &dummy);
-    p.items[2 * idx] = make_int4(b, g, rb, split);
-    p.items[2 * idx + 1] = make_int4(t0, t1, P, 0);
-  };
-  if (sorted) {
-    // one thread per item: find its sequence by binary search over the bases
-    for (int idx = tid; idx < n_items; idx += nth) {
-      int a = 0, z = B - 1;
-      while (a < z) {
-        const int mid = (a + z + 1) >> 1;
-        if (s_base[mid] <= idx) a = mid;
-        else z = mid - 1;
-      }
-      write_item(idx, seq_at(a), idx - s_base[a]);
-    }
-  } else {
-    long long idx = off;  // this thread's first item (natural order)
-    for (int i = lo; i < hi; ++i) {
-      const int b = seq_at(i);
-      const int n = cdiv(tiles_of(b), CH) * per_seq;
-      for (int l = 0; l < n && idx < n_items; ++l, ++idx) write_item((int)idx, b, l);
+    const int sb = nch > 1 ? (small ? s_split[b] : p.split_base[b]) : -1;
+    const int n = nch * per_seq;
+    for (int l = 0; l < n && io < n_items; ++l, ++io) {
+      const int c = l / per_seq, rest = l % per_seq;
+      const int g = rest / p.n_rb, rb = rest % p.n_rb;
+      const int t0 = c * CH, t1e = min(nt, t0 + CH);
+      const int split = nch > 1 ? sb + (g * p.n_rb + rb) * nch + c : -1;
+      p.items[2 * io] = make_int4(b, g, rb, split);
+      p.items[2 * io + 1] = make_int4(t0, t1e, P, nch);
+      if (split >= 0 && split < p.split_cap)
+        p.slot_info[split] = make_int4(b, (g << 16) | rb, split - c, nch);
     }
   }
   if (tid == 0) {
     p.hdr->chunk_tiles = CH;
     p.hdr->n_items = n_items;
-    if (total > p.items_cap) atomicCAS(&p.hdr->status, 0, kErrWorkspace);
+    p.hdr->n_split_slots = (int)(all.x < p.split_cap ? all.x : p.split_cap);
+    if (all.x > p.split_cap || all.y > p.items_cap) atomicCAS(&p.hdr->status, 0, kErrWorkspace);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, attn_grid);
-  return cudaGetLastError();
+  int threads = p.mode == kModeDecode ? ((p.B + 31) / 32) * 32 : 32;
+  threads = threads < 128 ? 128 : (threads > kPlanThreads ? kPlanThreads : threads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, p, attn_grid);
 }
 
 }  // namespace bca
