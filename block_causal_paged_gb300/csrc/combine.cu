@@ -1,7 +1,7 @@
 // Split-KV combine for decode.
 //
 // A long prefix is split into chunks that different CTAs attend to (each
-// chunk is an online softmax over its keys, "Paged Attention"), so every row
+// chunk is an online softmax over its keys), so every row
 // of a split group has, per chunk c, a running maximum m_c (log2 units), a sum
 // l_c and an unnormalised output O_c.  Merging them is the same rescaling the
 // online softmax does between tiles:
@@ -9,9 +9,12 @@
 //
 // Work unit: one split group (its first slot in the slot table) x 32 head-dim
 // columns; 256 threads, one per row (two M-tiles of 128), so every load of a
-// partial is 512 contiguous bytes per warp and all chunks' loads of a unit are
-// in flight together.  Launched with programmatic dependent launch: the grid
-// may start while the attention kernel drains and waits for it to finish.
+// partial is 512 contiguous bytes per warp.  The (max, sum) pairs and partial
+// outputs of up to four chunks are loaded together and merged online (running
+// maximum, rescaled accumulator), so a unit costs about two memory round
+// trips.  One CTA per SM (about 200 registers per thread), grid-stride over
+// the units.  Launched with programmatic dependent launch: the grid may start
+// while the attention kernel drains and waits for it to finish.
 #include <cstdint>
 
 #include "bca_internal.h"
@@ -21,6 +24,7 @@ namespace {
 
 constexpr int kCombineThreads = 256;  // rows of a split group
 constexpr int kCols = 32;             // head-dim columns per work unit
+constexpr int kBatch = 4;             // chunks whose loads are in flight together
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -51,34 +55,51 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     const int tok = rb * 2 * p.tpm + m * p.tpm + r / p.hpr;
     if (r >= p.hpr * p.tpm || tok >= p.Dblk) continue;
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, ml[(size_t)(s + c) * 256 + R].x);
-    float den = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const float2 v = ml[(size_t)(s + c) * 256 + R];
-      den += (v.x == -INFINITY ? 0.f : ex2f(v.x - M)) * v.y;
-    }
-    const float inv = den > 0.f ? 1.0f / den : 0.f;
+    const float4* po = reinterpret_cast<const float4*>(p.part_o);
+    // online merge, kBatch chunks per round with all their loads in flight
+    float M = -INFINITY, den = 0.f;
     float acc[kCols];
 #pragma unroll
     for (int k = 0; k < kCols; ++k) acc[k] = 0.f;
-    const float4* po = reinterpret_cast<const float4*>(p.part_o);
-#pragma unroll 2
-    for (int c = 0; c < nch; ++c) {
-      const float mc = ml[(size_t)(s + c) * 256 + R].x;
-      const float w = mc == -INFINITY ? 0.f : ex2f(mc - M);
-      const float4* src = po + ((size_t)(s + c) * (HD / 4) + q * (kCols / 4)) * 256 + R;
-      float4 v[kCols / 4];
+    for (int c0 = 0; c0 < nch; c0 += kBatch) {
+      float2 mlv[kBatch];
+      float4 v[kBatch][kCols / 4];
 #pragma unroll
-      for (int k4 = 0; k4 < kCols / 4; ++k4) v[k4] = src[(size_t)k4 * 256];
+      for (int k = 0; k < kBatch; ++k) {
+        if (c0 + k < nch) {
+          const size_t slot = (size_t)(s + c0 + k);
+          mlv[k] = ml[slot * 256 + R];
+          const float4* src = po + (slot * (HD / 4) + q * (kCols / 4)) * 256 + R;
 #pragma unroll
-      for (int k4 = 0; k4 < kCols / 4; ++k4) {
-        acc[4 * k4 + 0] += w * v[k4].x;
-        acc[4 * k4 + 1] += w * v[k4].y;
-        acc[4 * k4 + 2] += w * v[k4].z;
-        acc[4 * k4 + 3] += w * v[k4].w;
+          for (int k4 = 0; k4 < kCols / 4; ++k4) v[k][k4] = src[(size_t)k4 * 256];
+        } else {
+          mlv[k] = make_float2(-INFINITY, 0.f);
+        }
       }
+      float Mn = M;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) Mn = fmaxf(Mn, mlv[k].x);
+      if (Mn == -INFINITY) continue;  // no key seen yet
+      const float a = M == -INFINITY ? 0.f : ex2f(M - Mn);
+      den *= a;
+#pragma unroll
+      for (int k = 0; k < kCols; ++k) acc[k] *= a;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (c0 + k >= nch) break;
+        const float w = mlv[k].x == -INFINITY ? 0.f : ex2f(mlv[k].x - Mn);
+        den += w * mlv[k].y;
+#pragma unroll
+        for (int k4 = 0; k4 < kCols / 4; ++k4) {
+          acc[4 * k4 + 0] += w * v[k][k4].x;
+          acc[4 * k4 + 1] += w * v[k][k4].y;
+          acc[4 * k4 + 2] += w * v[k][k4].z;
+          acc[4 * k4 + 3] += w * v[k][k4].w;
+        }
+      }
+      M = Mn;
     }
+    const float inv = den > 0.f ? 1.0f / den : 0.f;
     uint16_t* dst = p.out +
                     ((size_t)(b * p.Dblk + tok) * p.Hq + g * p.G + (r % p.hpr)) * HD + q * kCols;
 #pragma unroll
@@ -98,7 +119,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
 cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, int n_sms,
                                   cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (n_sms > 0 ? n_sms : 1));
+  cfg.gridDim = dim3(n_sms > 0 ? n_sms : 1);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
