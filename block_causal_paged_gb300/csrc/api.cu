@@ -394,7 +394,7 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
   p.part_ml = (float*)((char*)ws + lay.ml_off);
   p.part_o = (float*)((char*)ws + lay.o_off);
   p.split_cap = lay.cap;
-  // the commit of the block runs inside the attention kernel (its warp 2)
+  // the commit of the block runs in the epilogue kernel, after the attention
   p.commit_k = commit ? (uint16_t*)k_pool : nullptr;
   p.commit_v = commit ? (uint16_t*)v_pool : nullptr;
 
@@ -417,7 +417,8 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
     return BCA_ERR_CUDA;
   if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;
-  if (max_tiles > kChMin) {
+  // epilogue: the commit (if asked) and the split-KV combine (if any prefix can split)
+  if (commit || max_tiles > kChMin) {
     if (timed(BCA_KERNEL_COMBINE, s, [&] { return launch_decode_combine(p, HD, di.sms, s); }) != cudaSuccess)
       return BCA_ERR_CUDA;
   }

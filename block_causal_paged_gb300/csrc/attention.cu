@@ -216,6 +216,9 @@ struct Planner {
                                             const int (&koff)[kChunksPerTile]) {
     Rec* r = acquire();
     if (!r) return;
+    // the MMA warp never reads tile records: release this one on its behalf
+    // (counts toward the phase that frees the entry again)
+    if (lane == 0) mbar_arrive(&c.bar.rec_empty[idx % kNumRec]);
     if (lane == 0) {
       r->w[T_KIND] = kRecTile;
       r->w[T_SRC] = src;
@@ -766,10 +769,8 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p, int l
     if (!ok) break;
     const uint32_t ub = u;
     u += 2u * (uint32_t)n_t;
+    ri += (uint32_t)n_t;  // the item's tile records are released by the planner for this warp
     // tile 0: S for every active M-tile
-    if (!ring_get(c, p, ri)) break;
-    ring_release(c, ri, lane);
-    ++ri;
     uint32_t ks = ub % C::kStages;
     if (!wait_bar_warp(c, p, &c.bar.kv_full[ks], (ub / C::kStages) & 1)) break;
     tc_fence_after();
@@ -784,12 +785,14 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p, int l
     for (int j = 0; j < n_t && ok; ++j) {
       const uint32_t uv = ub + 2u * (uint32_t)j + 1u;
       const uint32_t vs = uv % C::kStages;
-      if (!(ok = wait_bar_warp(c, p, &c.bar.kv_full[vs], (uv / C::kStages) & 1))) break;
       const bool nxt = j + 1 < n_t;
+      // V(j) and K(j+1) are checked together, before the wait for P: their
+      // loads were issued tiles ago, and a satisfied wait still costs ~150
+      // cycles that are better spent while P is being computed
+      if (!(ok = wait_bar_warp(c, p, &c.bar.kv_full[vs], (uv / C::kStages) & 1))) break;
       if (nxt) {
-        if (!(ok = ring_get(c, p, ri) != nullptr)) break;
-        ring_release(c, ri, lane);
-        ++ri;
+        ks = (uv + 1u) % C::kStages;
+        if (!(ok = wait_bar_warp(c, p, &c.bar.kv_full[ks], ((uv + 1u) / C::kStages) & 1))) break;
       }
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
@@ -800,12 +803,6 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p, int l
         tc_fence_after();
         issue_pv<HD>(c, m, vs, j > 0);
         if (nxt) {
-          if (m == 0) {
-            const uint32_t uk = uv + 1u;
-            ks = uk % C::kStages;
-            if (!(ok = wait_bar_warp(c, p, &c.bar.kv_full[ks], (uk / C::kStages) & 1))) break;
-            tc_fence_after();
-          }
           issue_qk<HD>(c, m, ks);
           umma_commit(&c.bar.s_full[m]);
           if (j + 2 == n_t) umma_commit(&c.bar.q_empty[m]);  // last read of Q
@@ -822,58 +819,6 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p, int l
   // teardown: wait until every MMA issued by this warp has completed
   umma_commit(c.bar.drain);
   mbar_wait(c.bar.drain, 0, c.abort_flag, kWaitTimeoutCycles);
-}
-
-// ============================================================================
-// KV commit of a decode block (warp 2, idle after the TMEM allocation): the
-// block's rows P .. P+D-1 are copied from the dense block K/V into their
-// pages.  The attention of this step never reads pool rows at or after P
-// (full 16-key boxes lie below P, ragged ones are copied row by row up to
-// the last valid key), so the copy may run concurrently with it.
-// ============================================================================
-template <int HD>
-__device__ __forceinline__ void run_commit(const AttnParams& p, int lane) {
-  constexpr int kPerHead = HD / 8;  // 16-byte pieces per head row
-  const int D = p.Dblk, Hkv = p.Hkv, per_row = Hkv * kPerHead;
-  const long long rows = (long long)p.B * D;
-  const uint4* kd_src = reinterpret_cast<const uint4*>(p.k_dense);
-  const uint4* vd_src = reinterpret_cast<const uint4*>(p.v_dense);
-  uint4* kd = reinterpret_cast<uint4*>(p.commit_k);
-  uint4* vd = reinterpret_cast<uint4*>(p.commit_v);
-  // 32 rows per pass: lane l resolves the page of row base + l
-  for (long long base = blockIdx.x; base < rows; base += 32ll * gridDim.x) {
-    const long long my_row = base + (long long)lane * gridDim.x;
-    int my_page = -1, my_slot = 0;
-    if (my_row < rows) {
-      const int b = (int)(my_row / D), t = (int)(my_row % D);
-      const int P = __ldg(p.lens + b);
-      if (P >= 0 && P % D == 0 && (long long)P + D <= (long long)p.max_pages * p.S) {
-        const int pos = P + t;
-        const int page = __ldg(p.page_table + (size_t)b * p.max_pages + pos / p.S);
-        if (page >= 0 && page < p.num_pages) {
-          my_page = page;
-          my_slot = pos % p.S;
-        } else {
-          record_error(p, kErrPageOob);
-        }
-      }  // a bad prefix length is reported by the plan kernel
-    }
-    for (int j = 0; j < 32; ++j) {
-      const long long row = base + (long long)j * gridDim.x;
-      if (row >= rows) break;
-      const int page = __shfl_sync(0xffffffffu, my_page, j);
-      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-      if (page < 0) continue;
-      for (int i = lane; i < per_row; i += 32) {
-        const int h = i / kPerHead, cc = i % kPerHead;
-        const size_t dst = (((size_t)page * Hkv + h) * p.S + slot) * kPerHead + cc;
-        const uint4 kv = __ldg(kd_src + row * per_row + i);
-        const uint4 vv = __ldg(vd_src + row * per_row + i);
-        kd[dst] = kv;
-        vd[dst] = vv;
-      }
-    }
-  }
 }
 
 // ============================================================================
@@ -1141,8 +1086,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       run_loader<HD>(c, p, &tm_q, &tm_kp, &tm_vp, &tm_kd, &tm_vd, lane);
     } else if (warp == 1) {
       run_mma<HD>(c, p, lane);
-    } else if (p.commit_k != nullptr) {
-      run_commit<HD>(p, lane);
     }
     __syncwarp();
     regs_alloc<kRegsLaunch>();

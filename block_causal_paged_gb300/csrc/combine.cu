@@ -1,4 +1,12 @@
-// Split-KV combine for decode.
+// Decode epilogue kernel: the KV commit of the step's blocks and the split-KV
+// combine.
+//
+// Commit: the blocks' rows P .. P+D-1 are bit-copied from the dense block K/V
+// into their pages ("Inference for Interpretable Text-Diffusion Models", "KV
+// Cache": a final pass commits the block; "Paged Attention": position p lives
+// in page page_table[b][p / S], slot p % S); one warp per token row, 16-byte
+// accesses.  It runs after the attention kernel, which reads only rows below
+// P, and before anything later in the stream reads the pages.
 //
 // A long prefix is split into chunks that different CTAs attend to (each
 // chunk is an online softmax over its keys), so every row
@@ -38,10 +46,47 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
+// Commit of the blocks' K/V: warp w of the grid copies token rows w, w + W, ...
+template <int HD>
+__device__ __forceinline__ void commit_rows(const AttnParams& p) {
+  constexpr int kPerHead = HD / 8;  // 16-byte pieces per head row
+  const int lane = threadIdx.x & 31;
+  const int per_row = p.Hkv * kPerHead;
+  const long long rows = (long long)p.B * p.Dblk;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const uint4* ks = reinterpret_cast<const uint4*>(p.k_dense);
+  const uint4* vs = reinterpret_cast<const uint4*>(p.v_dense);
+  uint4* kd = reinterpret_cast<uint4*>(p.commit_k);
+  uint4* vd = reinterpret_cast<uint4*>(p.commit_v);
+  for (long long row = warp; row < rows; row += n_warps) {
+    const int b = (int)(row / p.Dblk), t = (int)(row % p.Dblk);
+    const int P = __ldg(p.lens + b);
+    if (P < 0 || P % p.Dblk != 0 || (long long)P + p.Dblk > (long long)p.max_pages * p.S)
+      continue;  // a bad prefix length is reported by the plan kernel
+    const int pos = P + t;
+    const int page = __ldg(p.page_table + (size_t)b * p.max_pages + pos / p.S);
+    if (page < 0 || page >= p.num_pages) {
+      if (lane == 0) atomicCAS(&p.hdr->status, 0, -16);  // page id outside the pool
+      continue;
+    }
+    const int slot = pos % p.S;
+    for (int i = lane; i < per_row; i += 32) {
+      const int h = i / kPerHead, cc = i % kPerHead;
+      const size_t dst = (((size_t)page * p.Hkv + h) * p.S + slot) * kPerHead + cc;
+      const uint4 kv = __ldg(ks + row * per_row + i);
+      const uint4 vv = __ldg(vs + row * per_row + i);
+      kd[dst] = kv;
+      vd[dst] = vv;
+    }
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (p.commit_k != nullptr) commit_rows<HD>(p);
   constexpr int kQ = HD / kCols;
   const int n_slots = *reinterpret_cast<volatile int*>(&p.hdr->n_split_slots);
   const int R = threadIdx.x;
