@@ -46,15 +46,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
-// Commit of the blocks' K/V: warp w of the grid copies token rows w, w + W, ...
+// Commit of the blocks' K/V by CTAs first_cta .. gridDim.x-1: their warp w
+// copies token rows w, w + W, ...
 template <int HD>
-__device__ __forceinline__ void commit_rows(const AttnParams& p) {
+__device__ __forceinline__ void commit_rows(const AttnParams& p, int first_cta) {
   constexpr int kPerHead = HD / 8;  // 16-byte pieces per head row
   const int lane = threadIdx.x & 31;
   const int per_row = p.Hkv * kPerHead;
   const long long rows = (long long)p.B * p.Dblk;
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long warp = ((long long)(blockIdx.x - first_cta) * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = ((long long)(gridDim.x - first_cta) * blockDim.x) >> 5;
   const uint4* ks = reinterpret_cast<const uint4*>(p.k_dense);
   const uint4* vs = reinterpret_cast<const uint4*>(p.v_dense);
   uint4* kd = reinterpret_cast<uint4*>(p.commit_k);
@@ -86,13 +87,19 @@ template <int HD>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (p.commit_k != nullptr) commit_rows<HD>(p);
   constexpr int kQ = HD / kCols;
   const int n_slots = *reinterpret_cast<volatile int*>(&p.hdr->n_split_slots);
+  // the two jobs are latency-bound: when both exist, half the CTAs do each
+  const bool commit = p.commit_k != nullptr, combine = n_slots > 0;
+  const int n_comb = combine ? (commit ? (int)gridDim.x / 2 : (int)gridDim.x) : 0;
+  if (commit && (int)blockIdx.x >= n_comb) {
+    commit_rows<HD>(p, n_comb);
+    return;
+  }
   const int R = threadIdx.x;
   const int m = R / kRowsPerMTile, r = R % kRowsPerMTile;
   const long long units = (long long)n_slots * kQ;
-  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+  for (long long u = blockIdx.x; u < units; u += n_comb) {
     const int s = (int)(u / kQ), q = (int)(u % kQ);
     const int4 info = p.slot_info[s];
     if (info.z != s) continue;  // only the first slot of a group does its work
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
 cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, int n_sms,
                                   cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_sms > 0 ? n_sms : 1);
+  cfg.gridDim = dim3(n_sms > 1 ? n_sms : 2);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

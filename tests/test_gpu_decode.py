@@ -1,4 +1,4 @@
-"""GPU parity of bca_decode (and its fused commit) against the fp64 oracle."""
+"""GPU parity of bca_decode (and its commit) against the fp64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -101,6 +101,27 @@ def test_split_kv_matches_unsplit(cuda_lib):
     b = r.run(ws=small).clone()
     assert bca.read_device_status(small) == 0
     assert_close(b, ref, what="unsplit")
+
+
+def test_serving_batch64_commit_bit_exact(cuda_lib):
+    """The step with commit on, at the benchmarked size: every page of the pool
+    equals the oracle's commit (blocks written at P .. P+D-1, everything else
+    untouched), and the attention output is unaffected by the commit."""
+    case = workloads.serving_decode(seed=3, D=64)
+    r = DecodeRun(case)
+    out = r.run(commit=True).clone()
+    assert r.status() == 0
+    S = case.pool.page_size
+    for name, pool, blk in (("k", r.k_pool, case.k_blk), ("v", r.v_pool, case.v_blk)):
+        src = (case.pool.k_pool if name == "k" else case.pool.v_pool).view(torch.int16).numpy()
+        want = oracle.commit(src, case.pool.page_table, case.prefix_len,
+                             blk.view(torch.int16).numpy(), case.D, S)
+        assert np.array_equal(pool.cpu().view(torch.int16).numpy(), want), name
+    P = np.array(case.prefix_len)
+    seqs = sorted(set([int(P.argmax()), int(P.argmin())]))
+    ref = _ref(case, seqs=seqs)
+    for b in seqs:
+        assert_close(out[b], ref[b], what=f"serving with commit, seq {b}")
 
 
 @pytest.mark.parametrize("D", [64, 32])
