@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   __shared__ int s_P[kPlanSortMax];      // prefix length per sequence
   __shared__ int s_ord[kPlanSortMax];    // schedule position -> sequence
   __shared__ int s_split[kPlanSortMax];  // first split slot per sequence
+  __shared__ int s_base[kPlanSortMax];   // first item of each schedule position
   __shared__ longlong2 s_red[32];
   const int tid = threadIdx.x;
   const int nth = blockDim.x;
@@ -145,8 +146,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   if (ch < 1) ch = 1;
   for (int guard = 0; guard < 40; ++guard) {
     long long ns = 0, ni = 0;
+    const int ch32 = (int)(ch < (1ll << 30) ? ch : (1ll << 30));  // tiles per sequence < 2^30
     for (int b = tid; b < B; b += nth) {
-      const long long nch = (tiles_of(b) + ch - 1) / ch;
+      const int nch = cdiv(tiles_of(b), ch32);
       ni += nch;
       if (nch > 1) ns += nch;
     }
@@ -183,33 +185,52 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   }
   longlong2 all;
   const longlong2 off = block_scan2(ls, li, s_red, &all);
-  long long so = off.x;
+  long long so = off.x, ib = off.y;
   for (int b = lo; b < hi; ++b) {
-    if (small) s_split[b] = (int)so;
+    if (small) {
+      s_split[b] = (int)so;
+      s_base[b] = (int)ib;  // position b of the schedule
+    }
     p.split_base[b] = (int)so;
     const int nch = cdiv(tiles_of(b), CH);
     if (nch > 1) so += (long long)nch * per_seq;
+    ib += (long long)cdiv(tiles_of(seq_at(b)), CH) * per_seq;
   }
   const int n_items = (int)(all.y < p.items_cap ? all.y : p.items_cap);
   __syncthreads();  // split bases visible to the block
 
-  // 5. items: each thread writes those of the sequences at its positions
-  long long io = off.y;
-  for (int i = lo; i < hi; ++i) {
-    const int b = seq_at(i);
+  // 5. items
+  auto write_item = [&](int io, int b, int l) {
     const int nt = tiles_of(b), P = prefix_of(b);
     const int nch = cdiv(nt, CH);
-    const int sb = nch > 1 ? (small ? s_split[b] : p.split_base[b]) : -1;
-    const int n = nch * per_seq;
-    for (int l = 0; l < n && io < n_items; ++l, ++io) {
-      const int c = l / per_seq, rest = l % per_seq;
-      const int g = rest / p.n_rb, rb = rest % p.n_rb;
-      const int t0 = c * CH, t1e = min(nt, t0 + CH);
-      const int split = nch > 1 ? sb + (g * p.n_rb + rb) * nch + c : -1;
-      p.items[2 * io] = make_int4(b, g, rb, split);
-      p.items[2 * io + 1] = make_int4(t0, t1e, P, nch);
-      if (split >= 0 && split < p.split_cap)
-        p.slot_info[split] = make_int4(b, (g << 16) | rb, split - c, nch);
+    const int c = l / per_seq, rest = l % per_seq;
+    const int g = rest / p.n_rb, rb = rest % p.n_rb;
+    const int t0 = c * CH, t1e = min(nt, t0 + CH);
+    const int split =
+        nch > 1 ? (small ? s_split[b] : p.split_base[b]) + (g * p.n_rb + rb) * nch + c : -1;
+    p.items[2 * io] = make_int4(b, g, rb, split);
+    p.items[2 * io + 1] = make_int4(t0, t1e, P, nch);
+    if (split >= 0 && split < p.split_cap)
+      p.slot_info[split] = make_int4(b, (g << 16) | rb, split - c, nch);
+  };
+  if (small) {
+    // one item per thread: its schedule position by binary search over the bases
+    for (int io = tid; io < n_items; io += nth) {
+      int a = 0, z = B - 1;
+      while (a < z) {
+        const int mid = (a + z + 1) >> 1;
+        if (s_base[mid] <= io) a = mid;
+        else z = mid - 1;
+      }
+      write_item(io, s_ord[a], io - s_base[a]);
+    }
+  } else {
+    // each thread writes the items of the sequences at its positions
+    long long io = off.y;
+    for (int i = lo; i < hi; ++i) {
+      const int b = seq_at(i);
+      const int n = cdiv(tiles_of(b), CH) * per_seq;
+      for (int l = 0; l < n && io < n_items; ++l, ++io) write_item((int)io, b, l);
     }
   }
   if (tid == 0) {
@@ -224,7 +245,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 
 cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream) {
   int threads = p.mode == kModeDecode ? ((p.B + 31) / 32) * 32 : 32;
-  threads = threads < 128 ? 128 : (threads > kPlanThreads ? kPlanThreads : threads);
+  threads = threads < 256 ? 256 : (threads > kPlanThreads ? kPlanThreads : threads);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(threads);
