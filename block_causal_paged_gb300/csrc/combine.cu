@@ -20,8 +20,8 @@
 // partial is 512 contiguous bytes per warp.  The (max, sum) pairs and partial
 // outputs of up to four chunks are loaded together and merged online (running
 // maximum, rescaled accumulator), so a unit costs about two memory round
-// trips.  One CTA per SM (about 200 registers per thread), grid-stride over
-// the units.  Launched with programmatic dependent launch: the grid may start
+// trips.  Two CTAs per SM; the combine CTAs read the slot table in
+// coalesced chunks and keep only the first slot of each group.  Launched with programmatic dependent launch: the grid may start
 // while the attention kernel drains and waits for it to finish.
 #include <cstdint>
 
@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kCombineThreads = 256;  // rows of a split group
 constexpr int kCols = 32;             // head-dim columns per work unit
-constexpr int kBatch = 4;             // chunks whose loads are in flight together
+constexpr int kBatch = 2;             // chunks whose loads are in flight together
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -96,72 +96,90 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     commit_rows<HD>(p, n_comb);
     return;
   }
-  const int R = threadIdx.x;
+  __shared__ int s_first[kCombineThreads];  // group starts of the current table chunk
+  __shared__ int s_wcnt[kCombineThreads / 32];
+  const int R = threadIdx.x, lane = R & 31, warp = R >> 5;
   const int m = R / kRowsPerMTile, r = R % kRowsPerMTile;
-  const long long units = (long long)n_slots * kQ;
-  for (long long u = blockIdx.x; u < units; u += n_comb) {
-    const int s = (int)(u / kQ), q = (int)(u % kQ);
-    const int4 info = p.slot_info[s];
-    if (info.z != s) continue;  // only the first slot of a group does its work
-    const int b = info.x, g = info.y >> 16, rb = info.y & 0xffff, nch = info.w;
-    const int tok = rb * 2 * p.tpm + m * p.tpm + r / p.hpr;
-    if (r >= p.hpr * p.tpm || tok >= p.Dblk) continue;
-    const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-    const float4* po = reinterpret_cast<const float4*>(p.part_o);
-    // online merge, kBatch chunks per round with all their loads in flight
-    float M = -INFINITY, den = 0.f;
-    float acc[kCols];
-#pragma unroll
-    for (int k = 0; k < kCols; ++k) acc[k] = 0.f;
-    for (int c0 = 0; c0 < nch; c0 += kBatch) {
-      float2 mlv[kBatch];
-      float4 v[kBatch][kCols / 4];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        if (c0 + k < nch) {
-          const size_t slot = (size_t)(s + c0 + k);
-          mlv[k] = ml[slot * 256 + R];
-          const float4* src = po + (slot * (HD / 4) + q * (kCols / 4)) * 256 + R;
-#pragma unroll
-          for (int k4 = 0; k4 < kCols / 4; ++k4) v[k][k4] = src[(size_t)k4 * 256];
-        } else {
-          mlv[k] = make_float2(-INFINITY, 0.f);
-        }
-      }
-      float Mn = M;
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) Mn = fmaxf(Mn, mlv[k].x);
-      if (Mn == -INFINITY) continue;  // no key seen yet
-      const float a = M == -INFINITY ? 0.f : ex2f(M - Mn);
-      den *= a;
-#pragma unroll
-      for (int k = 0; k < kCols; ++k) acc[k] *= a;
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        if (c0 + k >= nch) break;
-        const float w = mlv[k].x == -INFINITY ? 0.f : ex2f(mlv[k].x - Mn);
-        den += w * mlv[k].y;
-#pragma unroll
-        for (int k4 = 0; k4 < kCols / 4; ++k4) {
-          acc[4 * k4 + 0] += w * v[k][k4].x;
-          acc[4 * k4 + 1] += w * v[k][k4].y;
-          acc[4 * k4 + 2] += w * v[k][k4].z;
-          acc[4 * k4 + 3] += w * v[k][k4].w;
-        }
-      }
-      M = Mn;
+  // The slot table, 256 entries at a time: every combine CTA reads the chunk
+  // (one coalesced load), keeps the group starts, and takes its share of the
+  // (group, column slice) units.
+  for (int s0 = 0; s0 < n_slots; s0 += kCombineThreads) {
+    const int my_s = s0 + R;
+    const bool first = my_s < n_slots && p.slot_info[my_s].z == my_s;
+    const unsigned bal = __ballot_sync(0xffffffffu, first);
+    __syncthreads();  // the previous chunk's list is no longer read
+    if (lane == 0) s_wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, n_groups = 0;
+    for (int w = 0; w < kCombineThreads / 32; ++w) {
+      before += w < warp ? s_wcnt[w] : 0;
+      n_groups += s_wcnt[w];
     }
-    const float inv = den > 0.f ? 1.0f / den : 0.f;
-    uint16_t* dst = p.out +
-                    ((size_t)(b * p.Dblk + tok) * p.Hq + g * p.G + (r % p.hpr)) * HD + q * kCols;
-#pragma unroll
-    for (int k = 0; k < kCols; k += 8) {
-      uint4 o;
-      o.x = pack2(acc[k + 0] * inv, acc[k + 1] * inv);
-      o.y = pack2(acc[k + 2] * inv, acc[k + 3] * inv);
-      o.z = pack2(acc[k + 4] * inv, acc[k + 5] * inv);
-      o.w = pack2(acc[k + 6] * inv, acc[k + 7] * inv);
-      *reinterpret_cast<uint4*>(dst + k) = o;
+    if (first) s_first[before + __popc(bal & ((1u << lane) - 1))] = my_s;
+    __syncthreads();
+    for (int u = blockIdx.x; u < n_groups * kQ; u += n_comb) {
+      const int s = s_first[u / kQ], q = u % kQ;
+      const int4 info = p.slot_info[s];
+      const int b = info.x, g = info.y >> 16, rb = info.y & 0xffff, nch = info.w;
+      const int tok = rb * 2 * p.tpm + m * p.tpm + r / p.hpr;
+      if (r >= p.hpr * p.tpm || tok >= p.Dblk) continue;
+      const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+      const float4* po = reinterpret_cast<const float4*>(p.part_o);
+      // online merge, kBatch chunks per round with all their loads in flight
+      float M = -INFINITY, den = 0.f;
+      float acc[kCols];
+  #pragma unroll
+      for (int k = 0; k < kCols; ++k) acc[k] = 0.f;
+      for (int c0 = 0; c0 < nch; c0 += kBatch) {
+        float2 mlv[kBatch];
+        float4 v[kBatch][kCols / 4];
+  #pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (c0 + k < nch) {
+            const size_t slot = (size_t)(s + c0 + k);
+            mlv[k] = ml[slot * 256 + R];
+            const float4* src = po + (slot * (HD / 4) + q * (kCols / 4)) * 256 + R;
+  #pragma unroll
+            for (int k4 = 0; k4 < kCols / 4; ++k4) v[k][k4] = src[(size_t)k4 * 256];
+          } else {
+            mlv[k] = make_float2(-INFINITY, 0.f);
+          }
+        }
+        float Mn = M;
+  #pragma unroll
+        for (int k = 0; k < kBatch; ++k) Mn = fmaxf(Mn, mlv[k].x);
+        if (Mn == -INFINITY) continue;  // no key seen yet
+        const float a = M == -INFINITY ? 0.f : ex2f(M - Mn);
+        den *= a;
+  #pragma unroll
+        for (int k = 0; k < kCols; ++k) acc[k] *= a;
+  #pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (c0 + k >= nch) break;
+          const float w = mlv[k].x == -INFINITY ? 0.f : ex2f(mlv[k].x - Mn);
+          den += w * mlv[k].y;
+  #pragma unroll
+          for (int k4 = 0; k4 < kCols / 4; ++k4) {
+            acc[4 * k4 + 0] += w * v[k][k4].x;
+            acc[4 * k4 + 1] += w * v[k][k4].y;
+            acc[4 * k4 + 2] += w * v[k][k4].z;
+            acc[4 * k4 + 3] += w * v[k][k4].w;
+          }
+        }
+        M = Mn;
+      }
+      const float inv = den > 0.f ? 1.0f / den : 0.f;
+      uint16_t* dst = p.out +
+                      ((size_t)(b * p.Dblk + tok) * p.Hq + g * p.G + (r % p.hpr)) * HD + q * kCols;
+  #pragma unroll
+      for (int k = 0; k < kCols; k += 8) {
+        uint4 o;
+        o.x = pack2(acc[k + 0] * inv, acc[k + 1] * inv);
+        o.y = pack2(acc[k + 2] * inv, acc[k + 3] * inv);
+        o.z = pack2(acc[k + 4] * inv, acc[k + 5] * inv);
+        o.w = pack2(acc[k + 6] * inv, acc[k + 7] * inv);
+        *reinterpret_cast<uint4*>(dst + k) = o;
+      }
     }
   }
 }
@@ -171,7 +189,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
 cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, int n_sms,
                                   cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_sms > 1 ? n_sms : 2);
+  cfg.gridDim = dim3(2 * (n_sms > 0 ? n_sms : 1));  // two CTAs per SM
   cfg.blockDim = dim3(kCombineThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
