@@ -413,7 +413,10 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
       (long long)d->batch * d->num_kv_heads * p.n_rb * ceil_div_i(max_tiles, kChMin);
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
   cudaStream_t s = (cudaStream_t)stream;
-  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
+  // small batches are planned inside the attention kernel (no plan launch)
+  p.fused_plan = d->batch <= kFusedPlanMax ? 1 : 0;
+  if (!p.fused_plan &&
+      timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;
   if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;

@@ -54,6 +54,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max
 constexpr int kErrTimeout = -18;
 constexpr int kErrPageOob = -16;
 constexpr int kErrBadLength = -17;
+constexpr int kErrWorkspace = -4;
 
 enum RecKind : int { kRecItem = 0, kRecTile = 1, kRecEnd = 2 };
 
@@ -316,11 +317,124 @@ struct Planner {
   }
 
   // --------------------------------------------------------------------------
-  // Next work item from the shared counter (the plan kernel reset it).
+  // Next work item from the shared counter (zero at launch: the last CTA of
+  // the previous launch reset it, as does the plan kernel).
   __device__ int grab() {
     int idx = 0;
     if (lane == 0) idx = atomicAdd(&p.hdr->work_next, 1);
     return __shfl_sync(0xffffffffu, idx, 0);
+  }
+
+  // --------------------------------------------------------------------------
+  // Decode with at most kFusedPlanMax sequences: the planner warp of every CTA
+  // computes the plan itself, by the same rules as the plan kernel (chunk of
+  // about `waves` items per CTA, never below ch_min tiles and within the
+  // workspace; sequences longest first, ties by index; split slots in
+  // sequence order), holding sequences 2l and 2l+1 in lane l.  Every CTA gets
+  // the same plan; CTA 0 also writes the split tables the epilogue reads.
+  __device__ void run_decode_fused() {
+    const int B = p.B, D = p.Dblk, per_seq = p.Hkv * p.n_rb;
+    int P[2], nt[2], bad = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int b = 2 * lane + k;
+      P[k] = 0;
+      nt[k] = 0;  // no sequence
+      if (b < B) {
+        int v = __ldg(p.lens + b);
+        if (v < 0 || v % D != 0 || (long long)v + D > (long long)p.max_pages * p.S) {
+          bad = 1;  // treated as an empty prefix, reported in the status word
+          v = 0;
+        }
+        P[k] = v;
+        nt[k] = ceil_div(v, kTileKeys) + ceil_div(D, kTileKeys);
+      }
+    }
+    if (__any_sync(0xffffffffu, bad) && blockIdx.x == 0 && lane == 0)
+      record_error(p, kErrBadLength);
+    const long long tot = warp_sum_ll(nt[0] + nt[1]) * per_seq;
+    const long long target = (long long)gridDim.x * (p.waves > 0 ? p.waves : 1);
+    long long ch = (tot + target - 1) / target;
+    if (ch < p.ch_min) ch = p.ch_min;
+    if (ch < 1) ch = 1;
+    int CH = 1, nch[2] = {0, 0};
+    for (int guard = 0; guard < 40; ++guard) {
+      CH = (int)(ch < (1ll << 30) ? ch : (1ll << 30));
+      nch[0] = ceil_div(nt[0], CH);
+      nch[1] = ceil_div(nt[1], CH);
+      const long long ns =
+          warp_sum_ll((nch[0] > 1 ? nch[0] : 0) + (nch[1] > 1 ? nch[1] : 0)) * per_seq;
+      const long long ni = warp_sum_ll(nch[0] + nch[1]) * per_seq;
+      if (ns <= p.split_cap && ni <= p.items_cap) break;
+      ch *= 2;
+    }
+    // schedule position (rank) of each sequence, then its first item
+    int rank[2] = {0, 0}, base[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < kFusedPlanMax; ++j) {
+      const int ntj = __shfl_sync(0xffffffffu, nt[j & 1], j >> 1);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = 2 * lane + k;
+        rank[k] += (j < B) & ((ntj > nt[k]) | ((ntj == nt[k]) & (j < i)));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kFusedPlanMax; ++j) {
+      const int rj = __shfl_sync(0xffffffffu, rank[j & 1], j >> 1);
+      const int itj = __shfl_sync(0xffffffffu, nch[j & 1], j >> 1) * per_seq;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) base[k] += ((j < B) & (rj < rank[k])) ? itj : 0;
+    }
+    const long long n_all = warp_sum_ll(nch[0] + nch[1]) * per_seq;
+    const int n_items = (int)(n_all < p.items_cap ? n_all : p.items_cap);
+    // split slots, sequence order
+    const int sz0 = nch[0] > 1 ? nch[0] * per_seq : 0, sz1 = nch[1] > 1 ? nch[1] * per_seq : 0;
+    const int sb0 = (int)warp_excl_scan_ll(sz0 + sz1, lane);
+    const int sb[2] = {sb0, sb0 + sz0};
+    const long long n_slots = warp_sum_ll(sz0 + sz1);
+    if (blockIdx.x == 0) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int b = 2 * lane + k;
+        if (b >= B) continue;
+        p.split_base[b] = sb[k];
+        if (nch[k] <= 1) continue;
+        for (int gr = 0; gr < per_seq; ++gr) {
+          const int first = sb[k] + gr * nch[k];
+          for (int cc = 0; cc < nch[k]; ++cc)
+            if (first + cc < p.split_cap)
+              p.slot_info[first + cc] =
+                  make_int4(b, ((gr / p.n_rb) << 16) | (gr % p.n_rb), first, nch[k]);
+        }
+      }
+      if (lane == 0) {
+        p.hdr->chunk_tiles = CH;
+        p.hdr->n_items = n_items;
+        p.hdr->n_split_slots = (int)(n_slots < p.split_cap ? n_slots : p.split_cap);
+        if (n_slots > p.split_cap || n_all > p.items_cap) record_error(p, kErrWorkspace);
+      }
+    }
+    while (ok) {
+      const int idx = grab();
+      if (idx >= n_items) break;
+      const bool in0 = nch[0] > 0 && base[0] <= idx && idx < base[0] + nch[0] * per_seq;
+      const bool in1 = nch[1] > 0 && base[1] <= idx && idx < base[1] + nch[1] * per_seq;
+      const unsigned owners = __ballot_sync(0xffffffffu, in0 || in1);
+      const int o = __ffs(owners) - 1;
+      const int k = __shfl_sync(0xffffffffu, in1 ? 1 : 0, o);
+      const int b = 2 * o + k;
+      const int Pb = __shfl_sync(0xffffffffu, k ? P[1] : P[0], o);
+      const int ntb = __shfl_sync(0xffffffffu, k ? nt[1] : nt[0], o);
+      const int nchb = __shfl_sync(0xffffffffu, k ? nch[1] : nch[0], o);
+      const int sbb = __shfl_sync(0xffffffffu, k ? sb[1] : sb[0], o);
+      const int l = idx - __shfl_sync(0xffffffffu, k ? base[1] : base[0], o);
+      const int c = l / per_seq, rest = l % per_seq;
+      const int g = rest / p.n_rb, rb = rest % p.n_rb;
+      const int t0 = c * CH, t1 = min(ntb, t0 + CH);
+      const int split = nchb > 1 ? sbb + (g * p.n_rb + rb) * nchb + c : -1;
+      decode_item(b, Pb, g, rb, t0, t1, split);
+    }
   }
 
   // Decode items come from the plan kernel's list, longest sequences first:
@@ -543,7 +657,10 @@ struct Planner {
   }
 
   __device__ void run() {
-    if (p.mode == kModeDecode) run_decode();
+    if (p.mode == kModeDecode) {
+      if (p.fused_plan) run_decode_fused();
+      else run_decode();
+    }
     else if (p.mode == kModePrefill) run_prefill();
     else run_multicanvas();
     if (ok) emit_end();
@@ -565,7 +682,6 @@ __device__ __forceinline__ void ring_release(const Ctx& c, uint32_t i, int lane)
   __syncwarp();
   if (lane == 0) mbar_arrive(&c.bar.rec_empty[i % kNumRec]);
 }
-// Single-thread role (the MMA issuer).
 
 // ============================================================================
 // loader (warp 0)
@@ -1102,6 +1218,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(c.tmem, C::kTmemCols);
+  }
+  // The last CTA to leave resets the work counter for the next launch (every
+  // CTA has finished taking items by now).
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int done = atomicAdd(&p.hdr->exit_count, 1);
+    if (done == (int)gridDim.x - 1) {
+      p.hdr->work_next = 0;
+      p.hdr->exit_count = 0;
+      __threadfence();
+    }
   }
 }
 

@@ -13,6 +13,7 @@ constexpr int kChunkKeys = 16;    // keys per TMA box (a page holds whole chunks
 constexpr int kChunksPerTile = kTileKeys / kChunkKeys;
 constexpr int kRowsPerMTile = 128;
 constexpr int kThreads = 384;     // 12 warps, see the role map in attention.cu
+constexpr int kFusedPlanMax = 64; // decode batches up to this are planned inside the attention kernel
 // Per internal wait: about 2 s at the maximum SM clock (longer when clocked down).
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
@@ -27,8 +28,9 @@ struct WsHeader {
   unsigned long long tiles_full;
   unsigned long long tiles_partial;
   unsigned long long tiles_skipped;
-  int32_t n_split_slots;   // decode: split-KV slots in use (plan kernel)
-  int32_t reserved1[53];
+  int32_t n_split_slots;   // decode: split-KV slots in use (plan)
+  int32_t exit_count;      // attention CTAs finished in the current launch (reset by the last)
+  int32_t reserved1[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 constexpr size_t kWsHeaderBytes = 256;
@@ -55,6 +57,7 @@ struct AttnParams {
   int n_hp;            // prefill: M-tile pairs (heads) per KV head
   int n_rb;            // decode: row blocks per KV head (each = 2 M-tiles)
   int ch_min, waves;   // decode split policy
+  int fused_plan;      // decode: every CTA plans for itself (batch <= kFusedPlanMax)
   int n_qt_max;        // prefill: query tiles of the longest sequence (host bound)
   int n_rb_max;        // multicanvas: row blocks of the longest live list (host bound)
   float scale_log2;    // softmax scale * log2(e)

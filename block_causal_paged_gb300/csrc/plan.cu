@@ -105,7 +105,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   // (which may still be reading the workspace) before touching anything.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0) p.hdr->work_next = 0;
+  if (tid == 0) {
+    p.hdr->work_next = 0;
+    p.hdr->exit_count = 0;
+  }
   if (p.mode != kModeDecode) return;
 
   const int B = p.B;

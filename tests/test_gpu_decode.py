@@ -103,6 +103,27 @@ def test_split_kv_matches_unsplit(cuda_lib):
     assert_close(b, ref, what="unsplit")
 
 
+def test_batch96_planned_by_plan_kernel(cuda_lib):
+    """Batches above 64 are planned by the separate plan kernel (smaller ones
+    inside the attention kernel): same results, including split prefixes."""
+    rng = np.random.default_rng(12)
+    P = (rng.integers(0, 40, 96) * 64).tolist()
+    P[5] = 24576                                    # one long prefix: split into chunks
+    case = workloads.make_decode_case(P, D=64, Hq=16, Hkv=4, d=128, seed=12)
+    r = DecodeRun(case)
+    out = r.run(commit=True)
+    assert r.status() == 0
+    seqs = [0, 5, 37, 95]
+    ref = _ref(case, seqs=seqs)
+    for b in seqs:
+        assert_close(out[b], ref[b], what=f"batch 96 seq {b}")
+    S = case.pool.page_size
+    src = case.pool.k_pool.view(torch.int16).numpy()
+    want = oracle.commit(src, case.pool.page_table, case.prefix_len,
+                         case.k_blk.view(torch.int16).numpy(), case.D, S)
+    assert np.array_equal(r.k_pool.cpu().view(torch.int16).numpy(), want)
+
+
 def test_serving_batch64_commit_bit_exact(cuda_lib):
     """The step with commit on, at the benchmarked size: every page of the pool
     equals the oracle's commit (blocks written at P .. P+D-1, everything else
