@@ -17,6 +17,10 @@ bullet; "Inference: Fewer, smaller forwards", "Advancement 1" and
 "Advancement 13").  Keys are given in *logical* order with explicit
 positions; paging is a storage detail the oracle never sees.
 
+``confidence`` (the top prediction of a position and its probability under
+the softmax over the vocabulary) is the one entry point that is not an
+attention.
+
 Pins (tests/test_oracle_*.py) tie this code to things other than itself:
 brute-force per-row enumeration, PyTorch SDPA in fp64 for the special cases
 the pages reduce to (block size 1 = causal; one block = unmasked), closed
@@ -271,3 +275,34 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     u = f.view(np.uint32).astype(np.uint64)
     rounded = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
     return rounded.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def confidence(logits):
+    """Top prediction and its probability for each row of logits.
+
+    "Inference: Fewer, smaller forwards", "Advancement 2: tau_conf": on every
+    forward the model gives a distribution over the vocabulary at each
+    uncommitted position (the softmax of its logits), and the confidence is
+    the probability of the argmax, the top prediction; "Advancement 16" lists
+    the fused softmax-plus-argmax over the vocabulary that computes it.
+
+    logits [rows, vocab], any float dtype (read exactly as fp64).  Returns
+    (argmax int64 [rows], confidence fp64 [rows]).  Among equal maxima the
+    lowest index is the argmax.  Since the argmax holds the largest logit m,
+    its probability is exp(0) / sum_v exp(l_v - m) = 1 / sum_v exp(l_v - m).
+    A row whose logits are all -inf has no distribution: argmax 0,
+    confidence 0.
+    """
+    x = np.asarray(logits, dtype=np.float64)
+    if x.ndim != 2:
+        raise ValueError("logits must be [rows, vocab]")
+    rows = x.shape[0]
+    arg = np.zeros(rows, dtype=np.int64)
+    conf = np.zeros(rows, dtype=np.float64)
+    for r in range(rows):
+        m = x[r].max() if x.shape[1] else -math.inf
+        if m == -math.inf:
+            continue
+        arg[r] = int(np.argmax(x[r]))  # first occurrence of the maximum
+        conf[r] = 1.0 / np.exp(x[r] - m).sum()
+    return arg, conf
