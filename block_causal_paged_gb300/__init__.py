@@ -47,10 +47,10 @@ class Dims(ctypes.Structure):
 
 class KernelTimes(ctypes.Structure):
     """struct bca_kernel_times."""
-    _fields_ = [("launches", _i32 * 5), ("total_ms", ctypes.c_double * 5)]
+    _fields_ = [("launches", _i32 * 6), ("total_ms", ctypes.c_double * 6)]
 
 
-KERNEL_NAMES = ("attention", "combine", "commit", "promote", "plan")
+KERNEL_NAMES = ("attention", "combine", "commit", "promote", "plan", "confidence")
 
 _DP = ctypes.POINTER(Dims)
 SIGNATURES = {
@@ -71,6 +71,7 @@ SIGNATURES = {
                                 ctypes.c_int),
     "bca_decode_static_scratch": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                    _vp, _vp], ctypes.c_int),
+    "bca_confidence": ([_i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp], ctypes.c_int),
     "bca_profile_start": ([_i32], ctypes.c_int),
     "bca_profile_stop": ([ctypes.POINTER(KernelTimes)], ctypes.c_int),
 }
@@ -192,6 +193,22 @@ def bca_commit_kv(d: Dims, k_blk, v_blk, k_pool, v_pool, page_table, start_pos, 
                               _ptr(v_pool), _ptr(page_table), _ptr(start_pos), int(num_tokens),
                               _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "bca_commit_kv")
+
+
+DTYPE_BF16, DTYPE_F32 = 0, 1
+
+
+def bca_confidence(logits, argmax, conf, vocab: int | None = None, stream=None) -> None:
+    """Top prediction and its probability per row of `logits` ([rows, ld] bf16
+    or fp32 device tensor; the first `vocab` columns are the vocabulary)."""
+    import torch
+    rows, ld = logits.shape
+    dtype = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}.get(logits.dtype)
+    if dtype is None:
+        raise BcaError(ERR_INVALID_ARG, "bca_confidence: logits must be bf16 or fp32")
+    rc = load().bca_confidence(int(rows), int(ld if vocab is None else vocab), int(logits.stride(0)),
+                               dtype, _ptr(logits), _ptr(argmax), _ptr(conf), _stream(stream))
+    _check(rc, "bca_confidence")
 
 
 def bca_prefill(d: Dims, q, k, v, cu_seqlens, total_tokens: int, max_seqlen: int, k_pool, v_pool,

@@ -311,6 +311,28 @@ int bca_read_tile_counters(void* ws, int64_t counters[3], bca_stream_t stream) {
   return BCA_OK;
 }
 
+int bca_confidence(int64_t rows, int64_t vocab, int64_t ld, int dtype, const void* logits,
+                   int32_t* argmax, float* conf, bca_stream_t stream) {
+  if (rows < 0 || vocab < 1 || vocab >= (1ll << 31) || ld < vocab) return BCA_ERR_INVALID_ARG;
+  if (dtype != BCA_DTYPE_BF16 && dtype != BCA_DTYPE_F32) return BCA_ERR_INVALID_ARG;
+  if (rows == 0) return BCA_OK;
+  if (rows >= (1ll << 31)) return BCA_ERR_INVALID_ARG;  // one CTA per row
+  if (!logits || !argmax || !conf) return BCA_ERR_NULL;
+  const int esize = dtype == BCA_DTYPE_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(logits) % esize != 0 ||
+      reinterpret_cast<uintptr_t>(argmax) % 4 != 0 || reinterpret_cast<uintptr_t>(conf) % 4 != 0)
+    return BCA_ERR_ALIGN;
+  DeviceInfo di;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  return timed(BCA_KERNEL_CONFIDENCE, s, [&] {
+           return launch_confidence(rows, (int)vocab, ld, dtype, logits, argmax, conf, s);
+         }) == cudaSuccess
+             ? BCA_OK
+             : BCA_ERR_CUDA;
+}
+
 int bca_commit_kv(const bca_dims* d, const void* k_blk, const void* v_blk, void* k_pool,
                   void* v_pool, const int32_t* page_table, const int32_t* start_pos,
                   int32_t num_tokens, void* ws, size_t ws_bytes, bca_stream_t stream) {

@@ -104,6 +104,10 @@ cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head
 // over the slot table the plan kernel wrote.
 cudaError_t launch_decode_combine(const AttnParams& p, int head_dim, int n_sms, cudaStream_t stream);
 
+// Softmax-plus-argmax over the vocabulary (dtype 0: bf16, 1: fp32).
+cudaError_t launch_confidence(int64_t rows, int vocab, int64_t ld, int dtype, const void* logits,
+                              int32_t* argmax, float* conf, cudaStream_t stream);
+
 // Bit copy of K/V rows into pages.  Source rows are [rows, Hkv, d]; sequence
 // b owns rows src_first(b) .. src_first(b)+count(b)-1 and writes them to
 // logical positions start(b) .. start(b)+count(b)-1 of its pages.

@@ -157,6 +157,33 @@ int bca_decode(const bca_dims* dims, const void* q, const void* k_blk, const voi
                size_t workspace_bytes, bca_stream_t stream);
 
 /*
+ * bca_confidence -- the top prediction at each position and its probability.
+ *
+ * "Inference: Fewer, smaller forwards", "Advancement 2: tau_conf": on every
+ * forward the model gives a distribution over the vocabulary at each
+ * uncommitted position (the softmax of its logits); the confidence is the
+ * probability of the argmax, and a position commits when it clears tau_conf.
+ * "Advancement 16" lists the softmax-plus-argmax over the vocabulary as one
+ * fused pass.  For each row r, with m = max_v logits[r, v]:
+ *   argmax[r] = the lowest index v with logits[r, v] = m,
+ *   conf[r]   = 1 / sum_v exp(logits[r, v] - m).
+ * A row whose logits are all -inf gets argmax 0, conf 0; NaN logits give
+ * unspecified results.
+ *
+ * logits: [rows, vocab] with a row stride of ld elements (ld >= vocab), bf16
+ * (dtype BCA_DTYPE_BF16) or fp32 (BCA_DTYPE_F32), device memory aligned to
+ * its element size (rows whose start is 16-byte aligned are read fastest).
+ * argmax: int32 [rows]; conf: fp32 [rows]; device memory,
+ * written once per row.  1 <= vocab < 2^31.  Needs no workspace; asynchronous
+ * on `stream`; rows = 0 is a no-op.  Errors: BCA_ERR_INVALID_ARG (sizes,
+ * dtype), BCA_ERR_NULL, BCA_ERR_ALIGN, BCA_ERR_UNSUPPORTED, BCA_ERR_CUDA.
+ */
+#define BCA_DTYPE_BF16 0
+#define BCA_DTYPE_F32 1
+int bca_confidence(int64_t rows, int64_t vocab, int64_t ld, int dtype, const void* logits,
+                   int32_t* argmax, float* conf, bca_stream_t stream);
+
+/*
  * bca_commit_kv -- write finished K/V rows into their pages (a bit copy).
  *
  * "Inference for Interpretable Text-Diffusion Models", "KV Cache", step 3,
@@ -280,11 +307,12 @@ int bca_decode_static_scratch(const bca_dims* dims, const void* q, const void* k
  * use while a stream is being captured into a CUDA graph.
  */
 #define BCA_KERNEL_ATTENTION 0 /* the block-causal attention kernel */
-#define BCA_KERNEL_COMBINE 1   /* split-KV combine (decode) */
+#define BCA_KERNEL_COMBINE 1   /* decode epilogue: KV commit and split-KV combine */
 #define BCA_KERNEL_COMMIT 2    /* KV commit / prefill page write */
 #define BCA_KERNEL_PROMOTE 3   /* multicanvas arena promotion */
-#define BCA_KERNEL_PLAN 4      /* work planning before each attention launch */
-#define BCA_KERNEL_KINDS 5
+#define BCA_KERNEL_PLAN 4      /* work planning (prefill, multicanvas, decode batches > 64) */
+#define BCA_KERNEL_CONFIDENCE 5 /* softmax-plus-argmax over the vocabulary */
+#define BCA_KERNEL_KINDS 6
 
 typedef struct bca_kernel_times {
   int32_t launches[BCA_KERNEL_KINDS];

@@ -130,3 +130,21 @@ def test_product_package_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_confidence_argument_errors(bca):
+    """Host checks of bca_confidence that need no GPU."""
+    import ctypes
+    lib = bca.load()
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    f = lib.bca_confidence
+    assert f(4, 0, 8, 0, base, base, base, None) == bca.ERR_INVALID_ARG      # empty vocabulary
+    assert f(4, 8, 7, 0, base, base, base, None) == bca.ERR_INVALID_ARG      # ld < vocab
+    assert f(4, 8, 8, 3, base, base, base, None) == bca.ERR_INVALID_ARG      # unknown dtype
+    assert f(-1, 8, 8, 0, base, base, base, None) == bca.ERR_INVALID_ARG     # negative rows
+    assert f(0, 8, 8, 0, None, None, None, None) == bca.OK                   # no rows: no-op
+    assert f(4, 8, 8, 0, None, base, base, None) == bca.ERR_NULL
+    assert f(4, 8, 8, 0, base + 1, base, base, None) == bca.ERR_ALIGN        # bf16 logits at an odd byte
+    assert f(4, 8, 8, 1, base + 2, base, base, None) == bca.ERR_ALIGN        # fp32 logits at 2 bytes
+    assert f(4, 8, 8, 0, base, base + 2, base, None) == bca.ERR_ALIGN        # int32 argmax misaligned

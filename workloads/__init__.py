@@ -386,3 +386,22 @@ def prefill_4x8192(seed: int = 0, **kw) -> PrefillCase:
 
 def multicanvas_b16(seed: int = 0, **kw) -> MulticanvasCase:
     return make_multicanvas_case(16, 1024, 3, 256, Hq=32, Hkv=8, d=128, seed=seed, **kw)
+
+
+def confidence_logits(rows: int, vocab: int, seed: int = 0, dtype=None, device="cpu"):
+    """Synthetic language-model logits [rows, vocab] for the confidence pass:
+    N(0, 3) scores, and in every fourth row one token lifted by 6 to 14 (a
+    confident position), so both flat and peaked distributions occur.
+    Generated in fp32 from `seed` on `device` (a CPU draw and a device draw
+    of the same seed differ), then cast (bf16 by default)."""
+    import torch
+    if dtype is None:
+        dtype = torch.bfloat16
+    g = torch.Generator(device=device).manual_seed(int(seed) * 7919 + 17)
+    x = torch.randn((rows, vocab), generator=g, device=device) * 3.0
+    if rows and vocab:
+        peaked = torch.arange(0, rows, 4, device=device)
+        tok = torch.randint(0, vocab, (len(peaked),), generator=g, device=device)
+        lift = 6.0 + 8.0 * torch.rand((len(peaked),), generator=g, device=device)
+        x[peaked, tok] += lift
+    return x.to(dtype)
