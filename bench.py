@@ -411,6 +411,25 @@ def run_ours(args):
     st = bca.read_device_status(t["ws"])
     del t, case
 
+    # confidence of the top prediction at every position of the step's blocks
+    # (softmax-plus-argmax over a 262144-token vocabulary, bf16 logits)
+    conf_line = None
+    if not args.no_sweep:
+        rows, vocab = args.batch * args.D, 262144
+        lg = workloads.confidence_logits(rows, vocab, seed=args.seed + rank, device=dev)
+        c_arg = torch.empty(rows, dtype=torch.int32, device=dev)
+        c_conf = torch.empty(rows, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            bca.bca_confidence(lg, c_arg, c_conf)
+        c_steps = max(10, args.steps // 20)
+        c_ms = time_steps(torch, lambda: bca.bca_confidence(lg, c_arg, c_conf), c_steps, stream) / c_steps
+        c_bytes = rows * vocab * lg.element_size() + rows * 8
+        conf_line = {"rows": rows, "vocab": vocab, "dtype": "bf16", "us": c_ms * 1e3,
+                     "gbs": c_bytes / (c_ms * 1e-3) / 1e9,
+                     "frac": c_bytes / (c_ms * 1e-3) / 1e9 / pk["hbm_gbs"], "bound": "hbm",
+                     "algorithmic_bytes": c_bytes}
+        del lg
+
     sweep = []
     if not args.no_sweep:
         for D2 in (32, 64):
@@ -444,7 +463,7 @@ def run_ours(args):
                 "gpu_launches": int(round(launches_per_step * args.steps)),
                 "launches_per_step": launches_per_step,
                 "kernel_ms": {k: (v[1] / v[0] if v[0] else None) for k, v in prof.items()},
-                "clocks": clocks, "device_status": st, "sweep": sweep}
+                "clocks": clocks, "device_status": st, "sweep": sweep, "confidence": conf_line}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
