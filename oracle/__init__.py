@@ -103,6 +103,22 @@ def block_causal_mask(q_pos, k_pos, P0: int, D: int) -> np.ndarray:
     return mask
 
 
+def sliding_window_mask(q_pos, k_pos, window: int) -> np.ndarray:
+    """Dense [Tq, Tk] uint8 band of a sliding-window layer (1 = kept).
+
+    "Inference: Fewer, smaller forwards", "Advancement 11": arena entries keep
+    their absolute positions, so sliding-window layers can band-mask the
+    entries that fall outside the 1024-token window.  Reading: the window of a
+    query at position q holds the `window` most recent positions up to q,
+    i.e. a key at position k is kept iff q - k < window (keys after q, which
+    only the query's own canvas holds, are kept).  window <= 0: no band.
+    """
+    qp, kp = _i64(q_pos), _i64(k_pos)
+    if window <= 0:
+        return np.ones((qp.size, kp.size), dtype=np.uint8)
+    return (qp[:, None] - kp[None, :] < window).astype(np.uint8)
+
+
 def attention(q, k, v, q_pos, k_pos, P0: int, D: int, scale: float | None = None,
               nthreads: int | None = None, return_lse: bool = False, mask=None):
     """Block-causal attention of one sequence in fp64.
@@ -193,7 +209,7 @@ def prefill(q, k, v, cu_seqlens, D: int, scale=None, nthreads=None,
 
 def multicanvas(q_live, k_live, v_live, live_pos, live_count, k_arena: Sequence,
                 v_arena: Sequence, arena_pos: Sequence, prompt_len: int, canvas_len: int,
-                scale=None, nthreads=None, seqs: Sequence[int] | None = None):
+                scale=None, nthreads=None, seqs: Sequence[int] | None = None, window: int = 0):
     """Multi-canvas shrinking-window attention.
 
     "Inference: Fewer, smaller forwards", "Advancement 1", "Advancement 9",
@@ -203,7 +219,8 @@ def multicanvas(q_live, k_live, v_live, live_pos, live_count, k_arena: Sequence,
     arena (k_arena[b] with absolute positions arena_pos[b]) or is itself a
     live row.  P0 = prompt_len and D = canvas_len.
     q_live [B, max_live, Hq, d]; k_live/v_live [B, max_live, Hkv, d];
-    live_pos [B, max_live]; live_count [B].
+    live_pos [B, max_live]; live_count [B].  window > 0 adds the band of a
+    sliding-window layer (``sliding_window_mask``) to the block rule.
     Returns fp64 [B, max_live, Hq, d]; rows past live_count are NaN.
     """
     q_live, k_live, v_live = _f64(q_live), _f64(k_live), _f64(v_live)
@@ -217,8 +234,13 @@ def multicanvas(q_live, k_live, v_live, live_pos, live_count, k_arena: Sequence,
         keys = np.concatenate([ka, k_live[b, :n]], axis=0)
         vals = np.concatenate([va, v_live[b, :n]], axis=0)
         k_pos = np.concatenate([pa, live_pos[b, :n]])
+        mask = None
+        if window > 0:
+            mask = (block_causal_mask(live_pos[b, :n], k_pos, prompt_len, canvas_len)
+                    & sliding_window_mask(live_pos[b, :n], k_pos, window))
         out[b, :n] = attention(q_live[b, :n], keys, vals, live_pos[b, :n], k_pos,
-                               P0=prompt_len, D=canvas_len, scale=scale, nthreads=nthreads)
+                               P0=prompt_len, D=canvas_len, scale=scale, nthreads=nthreads,
+                               mask=mask)
     return out
 
 

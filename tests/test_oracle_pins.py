@@ -340,6 +340,41 @@ def test_multicanvas_arena_order_invariance():
     assert np.abs(a - b).max() < 1e-13
 
 
+@pytest.mark.parametrize("W", [1, 5, 17, 40])
+def test_sliding_window_multicanvas_is_a_windowed_prefix(W):
+    """"Advancement 11": a sliding-window layer band-masks the entries outside
+    the window.  With positions 0..N-1 in logical order, a live row at p sees
+    the contiguous slice [max(0, p - W + 1), lim(p)); evaluate it with
+    unmasked SDPA on that slice."""
+    c = workloads.make_multicanvas_case(2, 24, 3, 8, 4, 2, 16, seed=6, fill_bits_value=None)
+    got = oracle.multicanvas(c.q_live, c.k_live, c.v_live, c.live_pos, c.live_count, c.arena_k,
+                             c.arena_v, c.arena_pos, 24, 8, window=W)
+    for b in range(2):
+        n = int(c.live_count[b])
+        pos = torch.cat([c.arena_pos[b], c.live_pos[b, :n].long()])
+        keys = torch.cat([c.arena_k[b], c.k_live[b, :n]]).double()
+        vals = torch.cat([c.arena_v[b], c.v_live[b, :n]]).double()
+        order = torch.argsort(pos)
+        assert torch.equal(pos[order], torch.arange(24 + 24))
+        keys, vals = keys[order], vals[order]
+        for r in range(n):
+            p = int(c.live_pos[b, r])
+            lim = 24 + 8 * ((p - 24) // 8 + 1)
+            lo = max(0, p - W + 1)
+            ref = _sdpa(c.q_live[b, r:r + 1].double(), keys[lo:lim], vals[lo:lim]).numpy()
+            assert np.abs(got[b, r] - ref[0]).max() < 1e-13
+
+
+def test_window_wider_than_every_distance_is_no_band():
+    c = workloads.make_multicanvas_case(2, 24, 3, 8, 4, 2, 16, seed=7, fill_bits_value=None)
+    args = (c.q_live, c.k_live, c.v_live, c.live_pos, c.live_count, c.arena_k, c.arena_v,
+            c.arena_pos, 24, 8)
+    assert np.array_equal(oracle.multicanvas(*args), oracle.multicanvas(*args, window=48),
+                          equal_nan=True)
+    band = oracle.sliding_window_mask([10, 11], [0, 5, 9, 10, 11, 12], 3)
+    assert band.tolist() == [[0, 0, 1, 1, 1, 1], [0, 0, 1, 1, 1, 1]]
+
+
 # ---------------------------------------------------------------------------
 # 6. commit: a bit copy, checked against an independent flat-index scatter
 # ---------------------------------------------------------------------------
