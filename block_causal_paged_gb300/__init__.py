@@ -67,6 +67,8 @@ SIGNATURES = {
                     ctypes.c_int),
     "bca_multicanvas": ([_DP, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
                          _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "bca_multicanvas_window": ([_DP, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp,
+                                _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp], ctypes.c_int),
     "bca_validate_page_table": ([_DP, _vp, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)],
                                 ctypes.c_int),
     "bca_decode_static_scratch": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
@@ -223,7 +225,17 @@ def bca_prefill(d: Dims, q, k, v, cu_seqlens, total_tokens: int, max_seqlen: int
 def bca_multicanvas(d: Dims, q_live, k_live, v_live, live_pos, live_count, max_live: int,
                     prompt_len: int, n_canvas: int, k_pool, v_pool, page_table, kv_pos,
                     arena_len, commit_rows, commit_count, max_commit: int, out, workspace,
-                    stream=None) -> None:
+                    stream=None, window: int = 0) -> None:
+    """window > 0 calls bca_multicanvas_window (sliding-window layer)."""
+    if window:
+        rc = load().bca_multicanvas_window(
+            ctypes.byref(d), _ptr(q_live), _ptr(k_live), _ptr(v_live), _ptr(live_pos),
+            _ptr(live_count), int(max_live), int(prompt_len), int(n_canvas), int(window),
+            _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(kv_pos), _ptr(arena_len),
+            _ptr(commit_rows), _ptr(commit_count), int(max_commit), _ptr(out), _ptr(workspace),
+            workspace.numel(), _stream(stream))
+        _check(rc, "bca_multicanvas_window")
+        return
     rc = load().bca_multicanvas(ctypes.byref(d), _ptr(q_live), _ptr(k_live), _ptr(v_live),
                                 _ptr(live_pos), _ptr(live_count), int(max_live), int(prompt_len),
                                 int(n_canvas), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),

@@ -525,16 +525,18 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
   return BCA_OK;
 }
 
-int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
-                    const void* v_live, const int32_t* live_pos, const int32_t* live_count,
-                    int32_t max_live, int32_t prompt_len, int32_t n_canvas, void* k_pool,
-                    void* v_pool, const int32_t* page_table, int32_t* kv_pos,
-                    int32_t* arena_len, const int32_t* commit_rows,
-                    const int32_t* commit_count, int32_t max_commit, void* out, void* ws,
-                    size_t ws_bytes, bca_stream_t stream) {
+namespace {
+int multicanvas_impl(const bca_dims* d, const void* q_live, const void* k_live,
+                     const void* v_live, const int32_t* live_pos, const int32_t* live_count,
+                     int32_t max_live, int32_t prompt_len, int32_t n_canvas, void* k_pool,
+                     void* v_pool, const int32_t* page_table, int32_t* kv_pos,
+                     int32_t* arena_len, const int32_t* commit_rows,
+                     const int32_t* commit_count, int32_t max_commit, int32_t window, void* out,
+                     void* ws, size_t ws_bytes, bca_stream_t stream) {
   int rc = validate_dims(d);
   if (rc) return rc;
-  if (max_live < 0 || prompt_len < 0 || n_canvas < 1 || max_commit < 0) return BCA_ERR_INVALID_ARG;
+  if (max_live < 0 || prompt_len < 0 || n_canvas < 1 || max_commit < 0 || window < 0)
+    return BCA_ERR_INVALID_ARG;
   if ((long long)prompt_len + (long long)n_canvas * d->block_size >= (1ll << 31))
     return BCA_ERR_INVALID_ARG;
   if (d->batch == 0 || max_live == 0) return BCA_OK;
@@ -565,6 +567,7 @@ int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
   p.arena_len = arena_len;
   p.max_live = max_live;
   p.prompt_len = prompt_len;
+  p.window = window;
   p.k_pool = (const uint16_t*)k_pool;
   p.v_pool = (const uint16_t*)v_pool;
   p.k_dense = (const uint16_t*)k_live;
@@ -618,6 +621,32 @@ int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
     if (timed(BCA_KERNEL_PROMOTE, s, [&] { return launch_promote(c, s); }) != cudaSuccess) return BCA_ERR_CUDA;
   }
   return BCA_OK;
+}
+}  // namespace
+
+int bca_multicanvas(const bca_dims* d, const void* q_live, const void* k_live,
+                    const void* v_live, const int32_t* live_pos, const int32_t* live_count,
+                    int32_t max_live, int32_t prompt_len, int32_t n_canvas, void* k_pool,
+                    void* v_pool, const int32_t* page_table, int32_t* kv_pos,
+                    int32_t* arena_len, const int32_t* commit_rows,
+                    const int32_t* commit_count, int32_t max_commit, void* out, void* ws,
+                    size_t ws_bytes, bca_stream_t stream) {
+  return multicanvas_impl(d, q_live, k_live, v_live, live_pos, live_count, max_live, prompt_len,
+                          n_canvas, k_pool, v_pool, page_table, kv_pos, arena_len, commit_rows,
+                          commit_count, max_commit, 0, out, ws, ws_bytes, stream);
+}
+
+int bca_multicanvas_window(const bca_dims* d, const void* q_live, const void* k_live,
+                           const void* v_live, const int32_t* live_pos,
+                           const int32_t* live_count, int32_t max_live, int32_t prompt_len,
+                           int32_t n_canvas, int32_t window, void* k_pool, void* v_pool,
+                           const int32_t* page_table, int32_t* kv_pos, int32_t* arena_len,
+                           const int32_t* commit_rows, const int32_t* commit_count,
+                           int32_t max_commit, void* out, void* ws, size_t ws_bytes,
+                           bca_stream_t stream) {
+  return multicanvas_impl(d, q_live, k_live, v_live, live_pos, live_count, max_live, prompt_len,
+                          n_canvas, k_pool, v_pool, page_table, kv_pos, arena_len, commit_rows,
+                          commit_count, max_commit, window, out, ws, ws_bytes, stream);
 }
 
 int bca_validate_page_table(const bca_dims* d, const int32_t* pt, const int32_t* used,

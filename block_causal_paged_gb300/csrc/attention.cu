@@ -554,8 +554,8 @@ struct Planner {
 
   // Classify one arena tile (entries [128a, 128a+128) of sequence b):
   // returns 0 skip, 1 partial, 2 full; fills the chunk coordinates/offsets.
-  __device__ int arena_tile(int b, int A, int a, int g, int min_lim, int max_lim,
-                            int (&cd)[kChunksPerTile], int (&ko)[kChunksPerTile]) {
+  __device__ int arena_tile(int b, int A, int a, int g, int min_lim, int max_lim, int min_lo,
+                            int max_lo, int (&cd)[kChunksPerTile], int (&ko)[kChunksPerTile]) {
     constexpr int kLoads = kTileKeys / 32;
     int kmin = INT_MAX, kmax = INT_MIN, pg[kLoads];
 #pragma unroll
@@ -583,12 +583,21 @@ struct Planner {
       cd[i] = (e < A && page >= 0) ? (page * p.Hkv + g) * p.S + (e % p.S) : p.pool_rows;
       ko[i] = (e < A && page >= 0) ? page * p.S + (e % p.S) : 0;
     }
-    if (kmin >= max_lim) return 0;
-    if (kmax < min_lim && nvalid == kTileKeys) return 2;
+    return classify(kmin, kmax, nvalid, min_lim, max_lim, min_lo, max_lo);
+  }
+
+  // A tile of keys with positions in [kmin, kmax] against rows whose keys must
+  // lie in [lo(q), lim(q)): skipped (0) when no row sees any of them, full (2)
+  // when every row sees all of them and the tile holds 128 keys, else partial.
+  __device__ static int classify(int kmin, int kmax, int nvalid, int min_lim, int max_lim,
+                                 int min_lo, int max_lo) {
+    if (kmin >= max_lim || kmax < min_lo) return 0;
+    if (kmax < min_lim && kmin >= max_lo && nvalid == kTileKeys) return 2;
     return 1;
   }
 
-  __device__ int live_tile(int b, int n_live, int l, int min_lim, int max_lim) {
+  __device__ int live_tile(int b, int n_live, int l, int min_lim, int max_lim, int min_lo,
+                           int max_lo) {
     int kmin = INT_MAX, kmax = INT_MIN;
 #pragma unroll
     for (int h = 0; h < kTileKeys / 32; ++h) {
@@ -602,30 +611,34 @@ struct Planner {
     kmin = warp_min(kmin);
     kmax = warp_max(kmax);
     const int nvalid = min(kTileKeys, n_live - l * kTileKeys);
-    if (kmin >= max_lim) return 0;
-    if (kmax < min_lim && nvalid == kTileKeys) return 2;
-    return 1;
+    return classify(kmin, kmax, nvalid, min_lim, max_lim, min_lo, max_lo);
   }
 
   __device__ void multicanvas_item(int b, int n_live, int A, int g, int rb) {
     const int r0 = rb * 2 * p.tpm;
     const int nrows = min(2 * p.tpm, n_live - r0);
-    int lo = INT_MAX, hi = INT_MIN;
+    int lo = INT_MAX, hi = INT_MIN, qlo = INT_MAX, qhi = INT_MIN;
     for (int r = lane; r < nrows; r += 32) {
-      const int lim = row_limit(live_position(b, r0 + r), p.prompt_len, p.Dblk);
+      const int q = live_position(b, r0 + r);
+      const int lim = row_limit(q, p.prompt_len, p.Dblk);
       lo = min(lo, lim);
       hi = max(hi, lim);
+      qlo = min(qlo, q);
+      qhi = max(qhi, q);
     }
     const int min_lim = warp_min(lo), max_lim = warp_max(hi);
+    // sliding-window band: the keys of row q start at q - window + 1
+    const int min_lo = p.window > 0 ? warp_min(qlo) - p.window + 1 : INT_MIN;
+    const int max_lo = p.window > 0 ? warp_max(qhi) - p.window + 1 : INT_MIN;
     const int n_at = ceil_div(A, kTileKeys), n_lt = ceil_div(n_live, kTileKeys);
     // pass 1: count the tiles that are not fully excluded
     int n_tiles = 0;
     for (int a = 0; a < n_at; ++a) {
       int cd[kChunksPerTile], ko[kChunksPerTile];
-      if (arena_tile(b, A, a, g, min_lim, max_lim, cd, ko) != 0) ++n_tiles;
+      if (arena_tile(b, A, a, g, min_lim, max_lim, min_lo, max_lo, cd, ko) != 0) ++n_tiles;
     }
     for (int l = 0; l < n_lt; ++l)
-      if (live_tile(b, n_live, l, min_lim, max_lim) != 0) ++n_tiles;
+      if (live_tile(b, n_live, l, min_lim, max_lim, min_lo, max_lo) != 0) ++n_tiles;
     int qtok[2], qhead[2], ntok[2], qbase[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
@@ -642,12 +655,12 @@ struct Planner {
     // pass 2: emit
     for (int a = 0; a < n_at && ok; ++a) {
       int cd[kChunksPerTile], ko[kChunksPerTile];
-      const int cls = arena_tile(b, A, a, g, min_lim, max_lim, cd, ko);
+      const int cls = arena_tile(b, A, a, g, min_lim, max_lim, min_lo, max_lo, cd, ko);
       if (cls == 0) continue;
       emit_tile(0, cls == 2, min(kTileKeys, A - a * kTileKeys), g, 1, 0, cd, ko);
     }
     for (int l = 0; l < n_lt && ok; ++l) {
-      const int cls = live_tile(b, n_live, l, min_lim, max_lim);
+      const int cls = live_tile(b, n_live, l, min_lim, max_lim, min_lo, max_lo);
       if (cls == 0) continue;
       const int nvalid = min(kTileKeys, n_live - l * kTileKeys);
       const int kmode = p.live_pos ? 2 : 0;
@@ -940,7 +953,9 @@ __device__ __forceinline__ void run_mma(const Ctx& c, const AttnParams& p, int l
 // ============================================================================
 // softmax / epilogue (warps 4..11)
 // ============================================================================
-template <int HD>
+// kBand: the multicanvas sliding-window band (a per-row lower key bound);
+// a separate instantiation, so that the other modes keep their registers.
+template <int HD, bool kBand>
 __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, int m, int wq,
                                             int lane) {
   using C = Cfg<HD>;
@@ -964,10 +979,11 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
     const bool active = m < n_m;
     const int tok = r / p.hpr;
     const bool valid = active && r < p.hpr * p.tpm && tok < ntok;
-    int lim = INT_MAX;
+    int lim = INT_MAX, lo = INT_MIN;  // row q sees key positions in [lo, lim)
     if (valid) {
       const int qpos = qmode == 0 ? qbase + tok : __ldg(p.live_pos + qbase + tok);
       lim = row_limit(qpos, P0, Dblk);
+      if (kBand) lo = qpos - p.window + 1;
     }
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n_t; ++j) {
@@ -995,7 +1011,8 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
             else if (kmode == 1) kp = __ldg(p.kv_pos + koff[k >> 4] + (k & 15));
             else kp = __ldg(p.live_pos + kbase + k);
           }
-          if (!(kp < lim)) sv[k] = __float_as_uint(-INFINITY);
+          const bool seen = kBand ? (kp < lim && kp >= lo) : kp < lim;
+          if (!seen) sv[k] = __float_as_uint(-INFINITY);
         }
       }
       // row maximum of the raw scores (the scale is positive), in log2 units:
@@ -1108,7 +1125,7 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
 // ============================================================================
 // the kernel
 // ============================================================================
-template <int HD>
+template <int HD, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_kp,
@@ -1208,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_alloc<kRegsSoftmax>();
     named_barrier_sync(1, kThreads);
-    run_softmax<HD>(c, p, (warp - 4) >> 2, warp & 3, lane);
+    run_softmax<HD, kBand>(c, p, (warp - 4) >> 2, warp & 3, lane);
     __syncwarp();
     regs_dealloc<kRegsLaunch>();
   }
@@ -1232,19 +1249,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD>
+template <int HD, bool kBand>
 cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int grid,
                                 cudaStream_t stream) {
   using C = Cfg<HD>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD, kBand>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     // setmaxnreg.inc waits for registers released by setmaxnreg.dec; the
     // split must fit what the block is launched with, or the kernel would stall
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attention_kernel<HD>);
+    e = cudaFuncGetAttributes(&fa, attention_kernel<HD, kBand>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
     configured = true;
@@ -1259,7 +1276,7 @@ cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int g
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attention_kernel<HD>, maps.q, maps.kp, maps.vp, maps.kd,
+  return cudaLaunchKernelEx(&cfg, attention_kernel<HD, kBand>, maps.q, maps.kp, maps.vp, maps.kd,
                             maps.vd, p);
 }
 
@@ -1267,8 +1284,12 @@ cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int g
 
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head_dim, int grid,
                              cudaStream_t stream) {
-  if (head_dim == 128) return launch_attention_hd<128>(p, maps, grid, stream);
-  return launch_attention_hd<64>(p, maps, grid, stream);
+  const bool band = p.mode == kModeMulticanvas && p.window > 0;
+  if (head_dim == 128)
+    return band ? launch_attention_hd<128, true>(p, maps, grid, stream)
+                : launch_attention_hd<128, false>(p, maps, grid, stream);
+  return band ? launch_attention_hd<64, true>(p, maps, grid, stream)
+              : launch_attention_hd<64, false>(p, maps, grid, stream);
 }
 
 }  // namespace bca

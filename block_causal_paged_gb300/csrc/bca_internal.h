@@ -67,6 +67,7 @@ struct AttnParams {
   const int32_t* kv_pos;     // multicanvas arena positions [num_pages, S]
   const int32_t* arena_len;  // multicanvas
   int max_live, prompt_len;
+  int window;                // multicanvas: sliding-window band (key kept iff q - k < window); 0: none
   const uint16_t* k_pool;
   const uint16_t* v_pool;
   const uint16_t* k_dense;   // decode k_blk | prefill k | multicanvas k_live

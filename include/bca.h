@@ -254,6 +254,28 @@ int bca_multicanvas(const bca_dims* dims, const void* q_live, const void* k_live
                     void* workspace, size_t workspace_bytes, bca_stream_t stream);
 
 /*
+ * bca_multicanvas_window -- bca_multicanvas for a sliding-window layer.
+ *
+ * "Inference: Fewer, smaller forwards", "Advancement 11": the arena keeps
+ * each entry's absolute position, so a sliding-window attention layer can
+ * band-mask the entries that fall outside its window (1024 tokens in the
+ * pages' model), which lets up to 5 canvases run even when the prompt plus
+ * all canvases exceed the window.  A live row at position q sees a key at
+ * position k iff the bca_multicanvas rule holds and q - k < window (the
+ * window holds the `window` most recent positions up to q; later keys of
+ * the row's own canvas stay visible).  window = 0 is bca_multicanvas;
+ * window < 0 is BCA_ERR_INVALID_ARG.  All other arguments as bca_multicanvas.
+ */
+int bca_multicanvas_window(const bca_dims* dims, const void* q_live, const void* k_live,
+                           const void* v_live, const int32_t* live_pos,
+                           const int32_t* live_count, int32_t max_live, int32_t prompt_len,
+                           int32_t n_canvas, int32_t window, void* k_pool, void* v_pool,
+                           const int32_t* page_table, int32_t* kv_pos, int32_t* arena_len,
+                           const int32_t* commit_rows, const int32_t* commit_count,
+                           int32_t max_commit, void* out, void* workspace,
+                           size_t workspace_bytes, bca_stream_t stream);
+
+/*
  * bca_validate_page_table -- host-side debug check of a page table (HOST
  * pointers), for use outside the timed path ("Paged Attention": the page
  * table is used with stricter error checking).  For each sequence b the first

@@ -97,12 +97,13 @@ class MulticanvasRun:
                           case.pool.page_size, case.pool.num_pages, case.pool.max_pages_per_seq)
         self.ws = bca.new_workspace(self.d, bca.OP_MULTICANVAS, device=dev)
 
-    def run(self):
+    def run(self, window=0):
         c = self.case
         bca.bca_multicanvas(self.d, self.q, self.k, self.v, self.live_pos, self.live_count,
                             c.q_live.shape[1], c.prompt_len, c.n_canvas, self.k_pool, self.v_pool,
                             self.page_table, self.kv_pos, self.arena_len, self.commit_rows,
-                            self.commit_count, c.commit_rows.shape[1], self.out, self.ws)
+                            self.commit_count, c.commit_rows.shape[1], self.out, self.ws,
+                            window=window)
         torch.cuda.synchronize()
         return self.out
 

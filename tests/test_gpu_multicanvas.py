@@ -10,9 +10,9 @@ from _gpu_cases import MulticanvasRun, assert_close
 pytestmark = pytest.mark.gpu
 
 
-def _ref(c):
+def _ref(c, window=0):
     return oracle.multicanvas(c.q_live, c.k_live, c.v_live, c.live_pos, c.live_count, c.arena_k,
-                              c.arena_v, c.arena_pos, c.prompt_len, c.canvas_len)
+                              c.arena_v, c.arena_pos, c.prompt_len, c.canvas_len, window=window)
 
 
 def _live_mask(c):
@@ -89,3 +89,34 @@ def test_all_rows_live_one_canvas_is_block_decode(cuda_lib):
     assert r.status() == 0
     ref = oracle.decode(c.q_live, c.k_live, c.v_live, c.arena_k, c.arena_v)
     assert_close(out, ref, what="one canvas, all live")
+
+
+def test_sliding_window_five_canvases(cuda_lib):
+    """"Advancement 11": a 1024-token sliding-window layer over a 1024-token
+    prompt and 5 canvases of 256 (positions up to 2304): later canvases lose
+    the start of the prompt."""
+    c = workloads.make_multicanvas_case(4, 1024, 5, 256, Hq=32, Hkv=8, d=128, seed=21)
+    r = MulticanvasRun(c)
+    out = r.run(window=1024)
+    assert r.status() == 0
+    m = _live_mask(c)
+    assert_close(out.cpu()[torch.from_numpy(m)], _ref(c, 1024)[m], what="window 1024, 5 canvases")
+
+
+@pytest.mark.parametrize("window", [1, 64, 200])
+def test_sliding_window_small(cuda_lib, window):
+    c = workloads.make_multicanvas_case(3, 300, 4, 96, Hq=6, Hkv=2, d=64, seed=22)
+    r = MulticanvasRun(c)
+    out = r.run(window=window)
+    assert r.status() == 0
+    m = _live_mask(c)
+    assert_close(out.cpu()[torch.from_numpy(m)], _ref(c, window)[m], what=f"window {window}")
+
+
+def test_wide_window_equals_no_window(cuda_lib):
+    c = workloads.make_multicanvas_case(2, 200, 3, 64, Hq=8, Hkv=2, d=128, seed=23,
+                                        commit_frac=0.0)
+    a = MulticanvasRun(c).run().clone()
+    b = MulticanvasRun(c).run(window=10 ** 6).clone()
+    m = torch.from_numpy(_live_mask(c))
+    assert torch.equal(a.cpu()[m], b.cpu()[m])
