@@ -280,6 +280,83 @@ def time_steps(torch, fn, steps, stream):
     return start.elapsed_time(end)
 
 
+def other_rows(args, bca, workloads, torch, pk, dev, stream):
+    """The block-causal prefill (4 x 8192) and the multicanvas step (batch 16,
+    prompt 1024, 3 canvases of 256; and 5 canvases under a 1024-token sliding
+    window), each timed over repeated calls with CUDA events and set against
+    its roofline: algorithmic flops (every visible (query, key) pair costs 4d
+    per query head) and bytes (every input byte once, the output, page
+    writes)."""
+    res = {}
+
+    def roof(flops, bytes_, ms):
+        t_mem = bytes_ / (pk["hbm_gbs"] * 1e9)
+        t_flop = flops / (pk["bf16_tflops"] * 1e12)
+        return {"us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
+                "gbs": bytes_ / (ms * 1e-3) / 1e9,
+                "bound": "tensor" if t_flop >= t_mem else "hbm",
+                "frac": max(t_mem, t_flop) / (ms * 1e-3),
+                "algorithmic_flops": flops, "algorithmic_bytes": bytes_}
+
+    def time_calls(fn, n):
+        for _ in range(3):
+            fn()
+        return time_steps(torch, fn, n, stream) / n
+
+    # prefill: 4 sequences of 8192 tokens, D = 64, 32/8 heads, d = 128, pages written
+    c = workloads.prefill_4x8192(seed=args.seed)
+    d = bca.dims(len(c.seq_lens), c.D, c.Hq, c.Hkv, c.d, c.pool.page_size, c.pool.num_pages,
+                 c.pool.max_pages_per_seq)
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    cu, pt = c.cu_seqlens.to(dev), c.pool.page_table.to(dev)
+    kp, vp = c.pool.k_pool.to(dev), c.pool.v_pool.to(dev)
+    out = torch.empty_like(q)
+    ws = bca.new_workspace(d, bca.OP_PREFILL, device=dev)
+    T, L = sum(c.seq_lens), max(c.seq_lens)
+    ms = time_calls(lambda: bca.bca_prefill(d, q, k, v, cu, T, L, kp, vp, pt, out, ws), 10)
+    pairs = sum(c.D * c.D * (L // c.D) * (L // c.D + 1) // 2 for L in c.seq_lens)
+    flops = 4.0 * c.d * c.Hq * pairs
+    bytes_ = T * (2 * c.Hq + 2 * c.Hkv) * c.d * 2.0 + 2 * T * c.Hkv * c.d * 2.0
+    res["prefill"] = dict(roof(flops, bytes_, ms), workload="4 x 8192 tokens, D=64, 32/8 heads, "
+                          "d=128, K/V written to pages of 16")
+    del q, k, v, out, kp, vp, ws
+
+    def mc(case, window, name, desc):
+        dd = bca.dims(case.B, case.canvas_len, case.Hq, case.Hkv, case.d, case.pool.page_size,
+                      case.pool.num_pages, case.pool.max_pages_per_seq)
+        t = {"q": case.q_live.to(dev), "k": case.k_live.to(dev), "v": case.v_live.to(dev),
+             "lp": case.live_pos.to(dev), "lc": case.live_count.to(dev),
+             "kp": case.pool.k_pool.to(dev), "vp": case.pool.v_pool.to(dev),
+             "pt": case.pool.page_table.to(dev), "kvp": case.kv_pos.to(dev),
+             "al": case.arena_len.to(dev)}
+        o = torch.empty_like(t["q"])
+        w = bca.new_workspace(dd, bca.OP_MULTICANVAS, device=dev)
+        max_live = case.q_live.shape[1]
+        fn = lambda: bca.bca_multicanvas(dd, t["q"], t["k"], t["v"], t["lp"], t["lc"], max_live,
+                                         case.prompt_len, case.n_canvas, t["kp"], t["vp"], t["pt"],
+                                         t["kvp"], t["al"], None, None, 0, o, w, window=window)
+        ms2 = time_calls(fn, 20)
+        P0, C = case.prompt_len, case.canvas_len
+        pairs2 = 0
+        for b in range(case.B):
+            n = int(case.live_count[b])
+            qp = case.live_pos[b, :n].long()
+            lim = P0 + C * ((qp - P0) // C + 1)
+            lo = (qp - window + 1).clamp(min=0) if window > 0 else torch.zeros_like(qp)
+            pairs2 += int((lim - lo).sum())
+        flops2 = 4.0 * case.d * case.Hq * pairs2
+        A = int(case.arena_len.sum())
+        nl = int(case.live_count.sum())
+        bytes2 = (A + nl) * case.Hkv * case.d * 2 * 2.0 + 2 * nl * case.Hq * case.d * 2.0
+        res[name] = dict(roof(flops2, bytes2, ms2), workload=desc)
+
+    mc(workloads.multicanvas_b16(seed=args.seed), 0, "multicanvas",
+       "batch 16, prompt 1024, 3 canvases of 256 with 30-100% live rows, 32/8 heads, d=128")
+    mc(workloads.make_multicanvas_case(16, 1024, 5, 256, 32, 8, 128, seed=args.seed), 1024,
+       "multicanvas_window", "as above with 5 canvases under a 1024-token sliding window")
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -429,6 +506,7 @@ def run_ours(args):
                      "frac": c_bytes / (c_ms * 1e-3) / 1e9 / pk["hbm_gbs"], "bound": "hbm",
                      "algorithmic_bytes": c_bytes}
         del lg
+    rows_line = other_rows(args, bca, workloads, torch, pk, dev, stream) if not args.no_sweep else None
 
     sweep = []
     if not args.no_sweep:
@@ -463,7 +541,8 @@ def run_ours(args):
                 "gpu_launches": int(round(launches_per_step * args.steps)),
                 "launches_per_step": launches_per_step,
                 "kernel_ms": {k: (v[1] / v[0] if v[0] else None) for k, v in prof.items()},
-                "clocks": clocks, "device_status": st, "sweep": sweep, "confidence": conf_line}
+                "clocks": clocks, "device_status": st, "sweep": sweep, "confidence": conf_line,
+                "other_rows": rows_line}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
