@@ -224,6 +224,11 @@ DecodeWsLayout decode_ws_layout(int B, int Hkv, int n_rb, int head_dim, int n_sm
   return l;
 }
 
+size_t multicanvas_ws_bytes(int B, int max_pages, int S) {
+  const size_t n_at = ((size_t)max_pages * S + kTileKeys - 1) / kTileKeys;
+  return kWsHeaderBytes + round_up((size_t)(B > 0 ? B : 1) * n_at * sizeof(int2), 256);
+}
+
 size_t decode_ws_minimum(int B, int Hkv, int n_rb, int head_dim, int n_sms) {
   return decode_ws_layout(B, Hkv, n_rb, head_dim, n_sms, 0).slot_off;
 }
@@ -274,8 +279,9 @@ size_t bca_workspace_size(const bca_dims* d, int op) {
                ? decode_ws_recommended(d->batch, d->num_kv_heads, n_rb, d->head_dim, sms)
                : decode_ws_minimum(d->batch, d->num_kv_heads, n_rb, d->head_dim, sms);
   }
-  if (op == BCA_OP_PREFILL || op == BCA_OP_MULTICANVAS || op == BCA_OP_COMMIT)
-    return kWsHeaderBytes;
+  if (op == BCA_OP_MULTICANVAS)
+    return multicanvas_ws_bytes(d->batch, d->max_pages_per_seq, d->page_size);
+  if (op == BCA_OP_PREFILL || op == BCA_OP_COMMIT) return kWsHeaderBytes;
   return 0;
 }
 
@@ -549,7 +555,8 @@ int multicanvas_impl(const bca_dims* d, const void* q_live, const void* k_live,
     return BCA_ERR_ALIGN;
   const long long q_tokens = (long long)d->batch * max_live;
   if (q_tokens * d->num_q_heads >= (1ll << 31)) return BCA_ERR_INVALID_ARG;
-  if (ws_bytes < kWsHeaderBytes) return BCA_ERR_WORKSPACE;
+  if (ws_bytes < multicanvas_ws_bytes(d->batch, d->max_pages_per_seq, d->page_size))
+    return BCA_ERR_WORKSPACE;
   DeviceInfo di;
   if ((rc = device_info(&di))) return rc;
 
@@ -575,6 +582,8 @@ int multicanvas_impl(const bca_dims* d, const void* q_live, const void* k_live,
   p.dense_tokens = (int)q_tokens;
   p.out = (uint16_t*)out;
   p.hdr = (WsHeader*)ws;
+  p.tile_kv = (int2*)((char*)ws + kWsHeaderBytes);
+  p.n_at_max = ceil_div_i((long long)d->max_pages_per_seq * d->page_size, kTileKeys);
 
   AttnMaps maps;
   const int HD = d->head_dim;

@@ -552,38 +552,14 @@ struct Planner {
     if (bad && lane == 0) record_error(p, kErrBadLength);
   }
 
-  // Classify one arena tile (entries [128a, 128a+128) of sequence b):
-  // returns 0 skip, 1 partial, 2 full; fills the chunk coordinates/offsets.
-  __device__ int arena_tile(int b, int A, int a, int g, int min_lim, int max_lim, int min_lo,
-                            int max_lo, int (&cd)[kChunksPerTile], int (&ko)[kChunksPerTile]) {
-    constexpr int kLoads = kTileKeys / 32;
-    int kmin = INT_MAX, kmax = INT_MIN, pg[kLoads];
-#pragma unroll
-    for (int h = 0; h < kLoads; ++h) {
-      const int e = a * kTileKeys + 32 * h + lane;
-      pg[h] = -1;
-      if (e < A) {
-        const int page = page_of(b, e);
-        pg[h] = page;
-        if (page >= 0) {
-          const int pos = __ldg(p.kv_pos + (size_t)page * p.S + (e % p.S));
-          kmin = min(kmin, pos);
-          kmax = max(kmax, pos);
-        }
-      }
-    }
-    kmin = warp_min(kmin);
-    kmax = warp_max(kmax);
-    const int nvalid = min(kTileKeys, A - a * kTileKeys);
-#pragma unroll
-    for (int i = 0; i < kChunksPerTile; ++i) {
-      // chunk i starts at entry 16i: load i/2, lane 16*(i%2)
-      const int page = __shfl_sync(0xffffffffu, pg[i >> 1], 16 * (i & 1));
-      const int e = a * kTileKeys + i * kChunkKeys;
-      cd[i] = (e < A && page >= 0) ? (page * p.Hkv + g) * p.S + (e % p.S) : p.pool_rows;
-      ko[i] = (e < A && page >= 0) ? page * p.S + (e % p.S) : 0;
-    }
-    return classify(kmin, kmax, nvalid, min_lim, max_lim, min_lo, max_lo);
+  // Class of arena tile a (entries [128a, 128a+128) of sequence b; 0 past
+  // the last) from the plan kernel's {min, max} of its key positions.
+  __device__ int arena_class(int b, int A, int a, int n_at, int min_lim, int max_lim, int min_lo,
+                             int max_lo) const {
+    if (a >= n_at) return 0;
+    const int2 s = __ldcg(p.tile_kv + (size_t)b * p.n_at_max + a);
+    return classify(s.x, s.y, min(kTileKeys, A - a * kTileKeys), min_lim, max_lim, min_lo,
+                    max_lo);
   }
 
   // A tile of keys with positions in [kmin, kmax] against rows whose keys must
@@ -596,22 +572,37 @@ struct Planner {
     return 1;
   }
 
-  __device__ int live_tile(int b, int n_live, int l, int min_lim, int max_lim, int min_lo,
-                           int max_lo) {
-    int kmin = INT_MAX, kmax = INT_MIN;
+  // Classes of live tiles l0 .. l0+3 (0 past the last), two bits each; the
+  // positions of all four tiles are loaded before any is reduced.
+  __device__ uint32_t live_classes4(int b, int n_live, int l0, int min_lim, int max_lim,
+                                    int min_lo, int max_lo) {
+    constexpr int kPer = kTileKeys / 32;
+    int pos[4][kPer];
 #pragma unroll
-    for (int h = 0; h < kTileKeys / 32; ++h) {
-      const int r = l * kTileKeys + 32 * h + lane;
-      if (r < n_live) {
-        const int pos = live_position(b, r);
-        kmin = min(kmin, pos);
-        kmax = max(kmax, pos);
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int h = 0; h < kPer; ++h) {
+        const int r = (l0 + t) * kTileKeys + 32 * h + lane;
+        pos[t][h] = r < n_live ? live_position(b, r) : INT_MAX;
       }
+    uint32_t cls = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      int kmin = INT_MAX, kmax = INT_MIN;
+#pragma unroll
+      for (int h = 0; h < kPer; ++h) {
+        const int r = (l0 + t) * kTileKeys + 32 * h + lane;
+        kmin = min(kmin, pos[t][h]);
+        kmax = r < n_live ? max(kmax, pos[t][h]) : kmax;
+      }
+      kmin = warp_min(kmin);
+      kmax = warp_max(kmax);
+      const int nvalid = n_live - (l0 + t) * kTileKeys;
+      if (nvalid > 0)
+        cls |= (uint32_t)classify(kmin, kmax, min(kTileKeys, nvalid), min_lim, max_lim, min_lo,
+                                  max_lo) << (2 * t);
     }
-    kmin = warp_min(kmin);
-    kmax = warp_max(kmax);
-    const int nvalid = min(kTileKeys, n_live - l * kTileKeys);
-    return classify(kmin, kmax, nvalid, min_lim, max_lim, min_lo, max_lo);
+    return cls;
   }
 
   __device__ void multicanvas_item(int b, int n_live, int A, int g, int rb) {
@@ -631,14 +622,16 @@ struct Planner {
     const int min_lo = p.window > 0 ? warp_min(qlo) - p.window + 1 : INT_MIN;
     const int max_lo = p.window > 0 ? warp_max(qhi) - p.window + 1 : INT_MIN;
     const int n_at = ceil_div(A, kTileKeys), n_lt = ceil_div(n_live, kTileKeys);
-    // pass 1: count the tiles that are not fully excluded
+    // pass 1: count the tiles that are not fully excluded (arena tiles 32 at a
+    // time, one summary per lane; live tiles 4 at a time)
     int n_tiles = 0;
-    for (int a = 0; a < n_at; ++a) {
-      int cd[kChunksPerTile], ko[kChunksPerTile];
-      if (arena_tile(b, A, a, g, min_lim, max_lim, min_lo, max_lo, cd, ko) != 0) ++n_tiles;
+    for (int a0 = 0; a0 < n_at; a0 += 32)
+      n_tiles += __popc(__ballot_sync(
+          0xffffffffu, arena_class(b, A, a0 + lane, n_at, min_lim, max_lim, min_lo, max_lo) != 0));
+    for (int l0 = 0; l0 < n_lt; l0 += 4) {
+      const uint32_t c4 = live_classes4(b, n_live, l0, min_lim, max_lim, min_lo, max_lo);
+      n_tiles += __popc((c4 | (c4 >> 1)) & 0x55u);
     }
-    for (int l = 0; l < n_lt; ++l)
-      if (live_tile(b, n_live, l, min_lim, max_lim, min_lo, max_lo) != 0) ++n_tiles;
     int qtok[2], qhead[2], ntok[2], qbase[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
@@ -652,20 +645,51 @@ struct Planner {
     emit_item(n_tiles, n_m, p.live_pos ? 1 : 0, qtok, qhead, ntok, qbase, p.prompt_len, p.Dblk,
               -1);
     n_skip += (unsigned long long)(n_at + n_lt - n_tiles);
-    // pass 2: emit
-    for (int a = 0; a < n_at && ok; ++a) {
-      int cd[kChunksPerTile], ko[kChunksPerTile];
-      const int cls = arena_tile(b, A, a, g, min_lim, max_lim, min_lo, max_lo, cd, ko);
-      if (cls == 0) continue;
-      emit_tile(0, cls == 2, min(kTileKeys, A - a * kTileKeys), g, 1, 0, cd, ko);
+    // pass 2: emit.  Arena tiles: the chunk pages of the next four kept tiles
+    // are fetched at once (lane 8j + i: chunk i of the j-th).
+    constexpr int kTilesPerGroup = 32 / kChunksPerTile;
+    for (int a0 = 0; a0 < n_at && ok; a0 += 32) {
+      const int cls = arena_class(b, A, a0 + lane, n_at, min_lim, max_lim, min_lo, max_lo);
+      uint32_t keep = __ballot_sync(0xffffffffu, cls != 0);
+      const uint32_t full = __ballot_sync(0xffffffffu, cls == 2);
+      while (keep != 0 && ok) {
+        uint32_t mine = keep;
+        for (int k = 0; k < lane / kChunksPerTile; ++k) mine &= mine - 1;
+        int coord = p.pool_rows, koff = 0;  // out of range -> zero fill
+        if (mine != 0) {
+          const int e = (a0 + __ffs(mine) - 1) * kTileKeys + (lane % kChunksPerTile) * kChunkKeys;
+          if (e < A) {
+            const int page = page_of(b, e);
+            if (page >= 0) {
+              coord = (page * p.Hkv + g) * p.S + (e % p.S);
+              koff = page * p.S + (e % p.S);
+            }
+          }
+        }
+        const int ntile = min(kTilesPerGroup, __popc(keep));
+        for (int j = 0; j < ntile && ok; ++j) {
+          const int a = a0 + __ffs(keep) - 1;
+          keep &= keep - 1;
+          int cd[kChunksPerTile], ko[kChunksPerTile];
+#pragma unroll
+          for (int i = 0; i < kChunksPerTile; ++i) {
+            cd[i] = __shfl_sync(0xffffffffu, coord, kChunksPerTile * j + i);
+            ko[i] = __shfl_sync(0xffffffffu, koff, kChunksPerTile * j + i);
+          }
+          emit_tile(0, (full >> (a - a0)) & 1, min(kTileKeys, A - a * kTileKeys), g, 1, 0, cd, ko);
+        }
+      }
     }
-    for (int l = 0; l < n_lt && ok; ++l) {
-      const int cls = live_tile(b, n_live, l, min_lim, max_lim, min_lo, max_lo);
-      if (cls == 0) continue;
-      const int nvalid = min(kTileKeys, n_live - l * kTileKeys);
-      const int kmode = p.live_pos ? 2 : 0;
-      const int kbase = p.live_pos ? b * p.max_live + l * kTileKeys : p.prompt_len + l * kTileKeys;
-      emit_dense_tile(g, b * p.max_live + l * kTileKeys, nvalid, kmode, kbase, cls == 2);
+    const int kmode = p.live_pos ? 2 : 0;
+    for (int l0 = 0; l0 < n_lt && ok; l0 += 4) {
+      const uint32_t c4 = live_classes4(b, n_live, l0, min_lim, max_lim, min_lo, max_lo);
+      for (int t = 0; t < 4 && ok; ++t) {
+        const int cls = (c4 >> (2 * t)) & 3, l = l0 + t;
+        if (cls == 0) continue;
+        const int nvalid = min(kTileKeys, n_live - l * kTileKeys);
+        const int kbase = p.live_pos ? b * p.max_live + l * kTileKeys : p.prompt_len + l * kTileKeys;
+        emit_dense_tile(g, b * p.max_live + l * kTileKeys, nvalid, kmode, kbase, cls == 2);
+      }
     }
   }
 
@@ -699,16 +723,6 @@ __device__ __forceinline__ void ring_release(const Ctx& c, uint32_t i, int lane)
 // ============================================================================
 // loader (warp 0)
 // ============================================================================
-// f[T_COORD + i] for a runtime i < kChunksPerTile, without indexing the array
-// dynamically (that would place it in local memory).
-__device__ __forceinline__ int coord_of(const int (&f)[24], int i) {
-  int v = 0;
-#pragma unroll
-  for (int k = 0; k < kChunksPerTile; ++k)
-    if (k == i) v = f[T_COORD + k];
-  return v;
-}
-
 template <int HD>
 __device__ __forceinline__ void run_loader(const Ctx& c, const AttnParams& p, const CUtensorMap* tm_q,
                            const CUtensorMap* tm_kp, const CUtensorMap* tm_vp,
@@ -1003,16 +1017,38 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
       uint32_t sv[kTileKeys];
       tmem_ld128_sync(t_s, sv);
       if (!full) {
+        // key positions per 16-key chunk: consecutive (kmode 0), or 16
+        // consecutive entries of kv_pos (arena slots, kmode 1) or of
+        // live_pos (kmode 2), read as four 16-byte loads when aligned
 #pragma unroll
-        for (int k = 0; k < kTileKeys; ++k) {
-          int kp = INT_MAX;
-          if (k < nvalid) {
-            if (kmode == 0) kp = kbase + k;
-            else if (kmode == 1) kp = __ldg(p.kv_pos + koff[k >> 4] + (k & 15));
-            else kp = __ldg(p.live_pos + kbase + k);
+        for (int ch = 0; ch < kChunksPerTile; ++ch) {
+          const int k0 = ch * kChunkKeys;
+          int pos[kChunkKeys];
+#pragma unroll
+          for (int i = 0; i < kChunkKeys; ++i) pos[i] = kbase + k0 + i;
+          if (kmode != 0 && k0 < nvalid) {
+            const int32_t* src = kmode == 1 ? p.kv_pos + koff[ch] : p.live_pos + kbase + k0;
+            if (k0 + kChunkKeys <= nvalid && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+#pragma unroll
+              for (int q4 = 0; q4 < kChunkKeys / 4; ++q4) {
+                const int4 v4 = __ldg(reinterpret_cast<const int4*>(src) + q4);
+                pos[4 * q4] = v4.x;
+                pos[4 * q4 + 1] = v4.y;
+                pos[4 * q4 + 2] = v4.z;
+                pos[4 * q4 + 3] = v4.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < kChunkKeys; ++i)
+                pos[i] = k0 + i < nvalid ? __ldg(src + i) : INT_MAX;
+            }
           }
-          const bool seen = kBand ? (kp < lim && kp >= lo) : kp < lim;
-          if (!seen) sv[k] = __float_as_uint(-INFINITY);
+#pragma unroll
+          for (int i = 0; i < kChunkKeys; ++i) {
+            const int kp = k0 + i < nvalid ? pos[i] : INT_MAX;
+            const bool seen = kBand ? (kp < lim && kp >= lo) : kp < lim;
+            if (!seen) sv[k0 + i] = __float_as_uint(-INFINITY);
+          }
         }
       }
       // row maximum of the raw scores (the scale is positive), in log2 units:

@@ -87,14 +87,22 @@ struct AttnParams {
   // these pools by the attention kernel itself (null: no commit)
   uint16_t* commit_k;
   uint16_t* commit_v;
+  // multicanvas: {smallest, largest} key position of arena tile a of sequence
+  // b at tile_kv[b * n_at_max + a], written by the plan kernel
+  int2* tile_kv;
+  int n_at_max;              // arena tiles per sequence: ceil(max_pages * S / 128)
 };
+
+// Multicanvas workspace: header | arena tile summaries int2[B][n_at_max].
+size_t multicanvas_ws_bytes(int B, int max_pages, int S);
 
 struct AttnMaps {
   CUtensorMap q, kp, vp, kd, vd;
 };
 
 // Plan kernel: resets the work counter; for decode also chooses the split
-// chunk, orders sequences longest first and writes the item list.
+// chunk, orders sequences longest first and writes the item list; for
+// multicanvas summarizes the key positions of every arena tile.
 cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream);
 
 // Launch the block-causal attention kernel (decode, prefill or multicanvas).

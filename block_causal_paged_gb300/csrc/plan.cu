@@ -14,6 +14,13 @@
 //     {b, g << 16 | rb, first slot of its group, chunks} (read by the combine).
 // The block is sized to the batch (a multiple of 32 threads, at most 1024),
 // so small batches pay for few warps at every barrier.
+//
+// For a multicanvas step the plan is a summary of the arena instead: every
+// work item of a sequence (one per row block and KV head) classifies the
+// same arena tiles against its own rows, so the smallest and largest key
+// position of each tile are found once here rather than once per item.
+#include <algorithm>
+#include <climits>
 #include <cstdint>
 
 #include "bca_internal.h"
@@ -25,6 +32,8 @@ constexpr int kPlanThreads = 1024;  // upper bound; the launch uses fewer for sm
 constexpr int kPlanSortMax = 2048;  // larger batches keep their natural order
 constexpr int kErrBadLength = -17;
 constexpr int kErrWorkspace = -4;
+constexpr int kErrPageOob = -16;
+constexpr int kSummaryThreads = 256;
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -244,19 +253,77 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   }
 }
 
+// Multicanvas: tile_kv[b * n_at_max + a] = {min, max} of the key positions
+// kv_pos[page][slot] of arena entries 128a .. 128a+127 of sequence b (entry
+// e lives in page page_table[b][e / S], slot e % S).  Entries at or past
+// arena_len[b] do not count; nor do entries whose page id lies outside the
+// pool, which are reported (kErrPageOob) as the attention kernel would.  A
+// tile with no counted entry gets {INT_MAX, INT_MIN}, which every row skips.
+// One warp per tile, four entries per lane.
+__global__ void __launch_bounds__(kSummaryThreads) arena_summary_kernel(
+    const __grid_constant__ AttnParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    p.hdr->work_next = 0;
+    p.hdr->exit_count = 0;
+  }
+  const int lane = threadIdx.x & 31;
+  const long long n = (long long)p.B * p.n_at_max;
+  const long long stride = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n; w += stride) {
+    const int b = (int)(w / p.n_at_max), a = (int)(w % p.n_at_max);
+    int A = __ldg(p.arena_len + b);
+    if (A < 0 || (long long)A > (long long)p.max_pages * p.S) A = 0;  // reported by the attention kernel
+    int kmin = INT_MAX, kmax = INT_MIN, bad = 0;
+#pragma unroll
+    for (int h = 0; h < kTileKeys / 32; ++h) {
+      const int e = a * kTileKeys + 32 * h + lane;
+      if (e < A) {
+        const int page = __ldg(p.page_table + (size_t)b * p.max_pages + e / p.S);
+        if (page >= 0 && page < p.num_pages) {
+          const int pos = __ldg(p.kv_pos + (size_t)page * p.S + e % p.S);
+          kmin = min(kmin, pos);
+          kmax = max(kmax, pos);
+        } else {
+          bad = 1;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(&p.hdr->status, 0, kErrPageOob);
+    if (lane == 0) p.tile_kv[w] = make_int2(kmin, kmax);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  if (p.mode == kModeMulticanvas) {
+    constexpr int kWarps = kSummaryThreads / 32;
+    const long long tiles = (long long)p.B * p.n_at_max;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min<long long>(std::max<long long>(1, (tiles + kWarps - 1) / kWarps), 4096));
+    cfg.blockDim = dim3(kSummaryThreads);
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, arena_summary_kernel, p);
+  }
   int threads = p.mode == kModeDecode ? ((p.B + 31) / 32) * 32 : 32;
   threads = threads < 256 ? 256 : (threads > kPlanThreads ? kPlanThreads : threads);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(threads);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
+  cfg.attrs = pdl;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, plan_kernel, p, attn_grid);
 }

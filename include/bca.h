@@ -112,7 +112,10 @@ const char* bca_status_string(int status);
  * partial results for splitting long prefixes across CTAs (split-KV).  Any
  * size between BCA_OP_DECODE_MIN (no partials: long prefixes are then not
  * split) and BCA_OP_DECODE (the recommended size) works; the plan kernel
- * splits only as far as the partials fit.  Other ops need only the header. */
+ * splits only as far as the partials fit.  Multicanvas: the header and, per
+ * sequence, 8 bytes for every 128 entries of page-table capacity (the key
+ * position range of each arena tile).  Prefill and commit need only the
+ * header. */
 size_t bca_workspace_size(const bca_dims* dims, int op);
 
 /* Zero the workspace header (status word, counters).  Call once after

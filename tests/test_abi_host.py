@@ -108,6 +108,19 @@ def test_workspace_size_grows_with_batch(bca):
     assert bca.workspace_size(_d(bca), bca.OP_PREFILL) == 256
 
 
+def test_multicanvas_workspace_holds_arena_tile_summaries(bca):
+    # header + 8 bytes per sequence and 128 entries of page-table capacity
+    d = _d(bca, batch=3, max_pages_per_seq=20)          # 20 pages of 16 = 320 entries -> 3 tiles
+    n = bca.workspace_size(d, bca.OP_MULTICANVAS)
+    assert n == 256 + (3 * 3 * 8 + 255) // 256 * 256
+    lib = bca.load()
+    buf = ctypes.create_string_buffer(256)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    rc = lib.bca_multicanvas(ctypes.byref(d), a, a, a, a, a, 32, 64, 2, a, a, a, a, a, None, None,
+                             0, a, a, n - 1, None)
+    assert rc == bca.ERR_WORKSPACE
+
+
 def test_validate_page_table(bca):
     d = _d(bca, batch=2, num_pages=8, max_pages_per_seq=4)
     pt = torch.tensor([[0, 1, 2, -1], [3, 4, -1, -1]], dtype=torch.int32)

@@ -120,3 +120,24 @@ def test_wide_window_equals_no_window(cuda_lib):
     b = MulticanvasRun(c).run(window=10 ** 6).clone()
     m = torch.from_numpy(_live_mask(c))
     assert torch.equal(a.cpu()[m], b.cpu()[m])
+
+
+def test_device_error_bad_arena_page_is_reported(cuda_lib):
+    """A page id outside the pool in a sequence's arena is reported in the
+    status word; the kernels skip it and the outputs stay finite."""
+    import block_causal_paged_gb300 as bca
+    c = workloads.make_multicanvas_case(3, 40, 4, 24, Hq=6, Hkv=2, d=64, seed=5)
+    r = MulticanvasRun(c, promote=False)
+    r.page_table[1, 0] = c.pool.num_pages + 3
+    out = r.run()
+    assert r.status() == bca.ERR_DEVICE_PAGE_OOB
+    assert torch.isfinite(out.float()).all()
+
+
+def test_device_error_bad_arena_length_is_reported(cuda_lib):
+    import block_causal_paged_gb300 as bca
+    c = workloads.make_multicanvas_case(3, 40, 4, 24, Hq=6, Hkv=2, d=64, seed=5)
+    r = MulticanvasRun(c, promote=False)
+    r.arena_len[2] = c.pool.max_pages_per_seq * c.pool.page_size + 16
+    r.run()
+    assert r.status() == bca.ERR_DEVICE_BAD_LENGTH
