@@ -1005,51 +1005,70 @@ __device__ __forceinline__ void run_softmax(const Ctx& c, const AttnParams& p, i
       if (!t) return;
       const int full = t->w[T_FULL], nvalid = t->w[T_NVALID], kmode = t->w[T_KMODE];
       const int kbase = t->w[T_KBASE];
-      int koff[kChunksPerTile];
+      // Partial tile: lane l fetches the positions of keys 4l .. 4l+3 now, so
+      // that the load is in flight while S is computed.  Keys are consecutive
+      // from kbase (kmode 0), 16 consecutive kv_pos entries per chunk from
+      // the chunk's offset (arena slots, kmode 1) or consecutive live_pos
+      // entries (kmode 2); keys at or past nvalid get INT_MAX (never seen).
+      int kp[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
+      if (!full && active) {
+        const int k4 = 4 * lane;
+        if (kmode == 0) {
 #pragma unroll
-      for (int i = 0; i < kChunksPerTile; ++i) koff[i] = t->w[T_KOFF + i];
+          for (int i = 0; i < 4; ++i) kp[i] = k4 + i < nvalid ? kbase + k4 + i : INT_MAX;
+        } else if (k4 < nvalid) {
+          const int32_t* src = kmode == 1
+                                   ? p.kv_pos + t->w[T_KOFF + k4 / kChunkKeys] + k4 % kChunkKeys
+                                   : p.live_pos + kbase + k4;
+          if (k4 + 4 <= nvalid && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+            const int4 v4 = __ldg(reinterpret_cast<const int4*>(src));
+            kp[0] = v4.x;
+            kp[1] = v4.y;
+            kp[2] = v4.z;
+            kp[3] = v4.w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kp[i] = k4 + i < nvalid ? __ldg(src + i) : INT_MAX;
+          }
+        }
+      }
       ring_release(c, ri, lane);
       ++ri;
       if (!active) continue;
       if (!wait_bar_warp(c, p, &c.bar.s_full[m], s_par & 1)) return;
       s_par ^= 1u;
       tc_fence_after();
+      // Partial tile: visibility of key k for this row is bit k/4 of vis[k%4].
+      // Rows with the same key range [lo, lim) share one mask: per distinct
+      // range in the warp, four ballots over the lanes' keys build it (rows of
+      // one canvas share lim; only the band's lo differs per token).  Built
+      // before S is read into registers, while they are free.
+      uint32_t vis[4] = {0u, 0u, 0u, 0u};
+      if (!full) {
+        bool done = !valid;  // rows past the item's tokens see nothing
+        while (true) {
+          const uint32_t pend = __ballot_sync(0xffffffffu, !done);
+          if (pend == 0u) break;
+          const int leader = __ffs(pend) - 1;
+          const int L = __shfl_sync(0xffffffffu, lim, leader);
+          const int Lo = kBand ? __shfl_sync(0xffffffffu, lo, leader) : INT_MIN;
+          uint32_t bl[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            bl[i] = __ballot_sync(0xffffffffu, kBand ? (kp[i] < L && kp[i] >= Lo) : kp[i] < L);
+          if (!done && lim == L && (!kBand || lo == Lo)) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vis[i] = bl[i];
+            done = true;
+          }
+        }
+      }
       uint32_t sv[kTileKeys];
       tmem_ld128_sync(t_s, sv);
       if (!full) {
-        // key positions per 16-key chunk: consecutive (kmode 0), or 16
-        // consecutive entries of kv_pos (arena slots, kmode 1) or of
-        // live_pos (kmode 2), read as four 16-byte loads when aligned
 #pragma unroll
-        for (int ch = 0; ch < kChunksPerTile; ++ch) {
-          const int k0 = ch * kChunkKeys;
-          int pos[kChunkKeys];
-#pragma unroll
-          for (int i = 0; i < kChunkKeys; ++i) pos[i] = kbase + k0 + i;
-          if (kmode != 0 && k0 < nvalid) {
-            const int32_t* src = kmode == 1 ? p.kv_pos + koff[ch] : p.live_pos + kbase + k0;
-            if (k0 + kChunkKeys <= nvalid && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-#pragma unroll
-              for (int q4 = 0; q4 < kChunkKeys / 4; ++q4) {
-                const int4 v4 = __ldg(reinterpret_cast<const int4*>(src) + q4);
-                pos[4 * q4] = v4.x;
-                pos[4 * q4 + 1] = v4.y;
-                pos[4 * q4 + 2] = v4.z;
-                pos[4 * q4 + 3] = v4.w;
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < kChunkKeys; ++i)
-                pos[i] = k0 + i < nvalid ? __ldg(src + i) : INT_MAX;
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < kChunkKeys; ++i) {
-            const int kp = k0 + i < nvalid ? pos[i] : INT_MAX;
-            const bool seen = kBand ? (kp < lim && kp >= lo) : kp < lim;
-            if (!seen) sv[k0 + i] = __float_as_uint(-INFINITY);
-          }
-        }
+        for (int k = 0; k < kTileKeys; ++k)
+          if (!((vis[k & 3] >> (k >> 2)) & 1u)) sv[k] = __float_as_uint(-INFINITY);
       }
       // row maximum of the raw scores (the scale is positive), in log2 units:
       // four chains of three-input maxima
