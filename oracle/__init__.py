@@ -179,6 +179,36 @@ def decode(q, k_blk, v_blk, k_prefix: Sequence, v_prefix: Sequence, scale=None,
     return out
 
 
+def extend(q, k_new, v_new, k_prefix: Sequence, v_prefix: Sequence, scale=None,
+           nthreads=None, seqs: Sequence[int] | None = None):
+    """Short causal extend of a batch over its cached prefix.
+
+    "Introspective Diffusion Language Model", "3.3 I-DLM Serving Stack" and
+    Appendix D: each step appends a few causal query tokens (2N - 1 for
+    fixed-query introspective decoding, at most 9 in the short-extend case)
+    that attend the whole paged prefix and, among themselves, strictly
+    causally.  q [B, n, Hq, d] are the new tokens at positions P_b .. P_b+n-1;
+    keys are the logical prefix 0 .. P_b-1 (k_prefix[b]) followed by the n
+    new keys (k_new[b]).  The causal rule is the block rule with blocks of
+    one token (P0 = P_b, D = 1): key j is visible to query i iff j <= i.
+    Unlike a diffusion block, P_b need not be a multiple of anything.
+    Returns fp64 [B, n, Hq, d] (rows of sequences not in ``seqs`` are NaN).
+    """
+    q, k_new, v_new = _f64(q), _f64(k_new), _f64(v_new)
+    B, n = q.shape[0], q.shape[1]
+    out = np.full(q.shape, np.nan, dtype=np.float64)
+    for b in (range(B) if seqs is None else seqs):
+        kp, vp = _f64(k_prefix[b]), _f64(v_prefix[b])
+        P = kp.shape[0]
+        keys = np.concatenate([kp, k_new[b]], axis=0)
+        vals = np.concatenate([vp, v_new[b]], axis=0)
+        k_pos = np.arange(P + n, dtype=np.int64)
+        q_pos = P + np.arange(n, dtype=np.int64)
+        out[b] = attention(q[b], keys, vals, q_pos, k_pos, P0=P, D=1, scale=scale,
+                           nthreads=nthreads)
+    return out
+
+
 def prefill(q, k, v, cu_seqlens, D: int, scale=None, nthreads=None,
             q_rows: dict | None = None):
     """Block-causal prefill of packed sequences.
