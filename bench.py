@@ -281,9 +281,9 @@ def time_steps(torch, fn, steps, stream):
 
 
 def other_rows(args, bca, workloads, torch, pk, dev, stream):
-    """The block-causal prefill (4 x 8192) and the multicanvas step (batch 16,
-    prompt 1024, 3 canvases of 256; and 5 canvases under a 1024-token sliding
-    window), each timed over repeated calls with CUDA events and set against
+    """The block-causal prefill (4 x 8192), the short causal extend (batch 64,
+    9 tokens) and the multicanvas step (batch 16, prompt 1024, 3 canvases of
+    256; and 5 canvases under a 1024-token sliding window), each timed over repeated calls with CUDA events and set against
     its roofline: algorithmic flops (every visible (query, key) pair costs 4d
     per query head) and bytes (every input byte once, the output, page
     writes)."""
@@ -349,6 +349,33 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         nl = int(case.live_count.sum())
         bytes2 = (A + nl) * case.Hkv * case.d * 2 * 2.0 + 2 * nl * case.Hq * case.d * 2.0
         res[name] = dict(roof(flops2, bytes2, ms2), workload=desc)
+
+    # short causal extend: batch 64, 9 new tokens (2N-1, N = 5), prefixes at
+    # token granularity, 32/8 heads, d = 128, the new rows committed
+    P = workloads.prefix_loguniform_blocks(64, 128, 32768, 1, seed=args.seed)
+    n = 9
+    ce = workloads.make_decode_case(P, D=n, Hq=32, Hkv=8, d=128, seed=args.seed,
+                                    keep_logical=False)
+    de = bca.dims(ce.B, n, ce.Hq, ce.Hkv, ce.d, ce.pool.page_size, ce.pool.num_pages,
+                  ce.pool.max_pages_per_seq)
+    te = {"q": ce.q.to(dev), "k": ce.k_blk.to(dev), "v": ce.v_blk.to(dev),
+          "kp": ce.pool.k_pool.to(dev), "vp": ce.pool.v_pool.to(dev),
+          "pt": ce.pool.page_table.to(dev),
+          "pl": torch.tensor(P, dtype=torch.int32, device=dev)}
+    oe = torch.empty_like(te["q"])
+    we = bca.new_workspace(de, bca.OP_DECODE, device=dev)
+    ms_e = time_calls(lambda: bca.bca_extend(de, te["q"], te["k"], te["v"], te["kp"], te["vp"],
+                                             te["pt"], te["pl"], oe, True, we), 20)
+    pairs_e = sum(p_ * n + n * (n + 1) // 2 for p_ in P)
+    flops_e = 4.0 * ce.d * ce.Hq * pairs_e
+    kv_row = 2 * ce.Hkv * ce.d * 2.0  # K and V bytes of one token
+    bytes_e = (sum(P) * kv_row + ce.B * n * (2 * ce.Hq * ce.d * 2.0 + 2 * kv_row)
+               + ce.B * ce.pool.max_pages_per_seq * 4.0)
+    res["extend"] = dict(roof(flops_e, bytes_e, ms_e),
+                         workload=f"batch 64, 9 new causal tokens after log-uniform prefixes in "
+                                  f"[128, 32768] (sum {sum(P)}), 32/8 heads, d=128, page 16, "
+                                  f"new rows committed")
+    del te, oe, we, ce
 
     mc(workloads.multicanvas_b16(seed=args.seed), 0, "multicanvas",
        "batch 16, prompt 1024, 3 canvases of 256 with 30-100% live rows, 32/8 heads, d=128")

@@ -62,6 +62,8 @@ SIGNATURES = {
     "bca_read_tile_counters": ([_vp, ctypes.POINTER(_i64), _vp], ctypes.c_int),
     "bca_decode": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp],
                    ctypes.c_int),
+    "bca_extend": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp],
+                   ctypes.c_int),
     "bca_commit_kv": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp], ctypes.c_int),
     "bca_prefill": ([_DP, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
                     ctypes.c_int),
@@ -174,6 +176,15 @@ def bca_decode(d: Dims, q, k_blk, v_blk, k_pool, v_pool, page_table, prefix_len,
                            _ptr(v_pool), _ptr(page_table), _ptr(prefix_len), _ptr(out),
                            1 if commit else 0, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "bca_decode")
+
+
+def bca_extend(d: Dims, q, k_new, v_new, k_pool, v_pool, page_table, prefix_len, out,
+               commit: bool, workspace, stream=None) -> None:
+    """Short causal extend: d.block_size new tokens per sequence (see include/bca.h)."""
+    rc = load().bca_extend(ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                           _ptr(v_pool), _ptr(page_table), _ptr(prefix_len), _ptr(out),
+                           1 if commit else 0, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "bca_extend")
 
 
 def bca_decode_static_scratch(d: Dims, q, k_blk, v_blk, k_pool, v_pool, page_table, prefix_len,

@@ -375,9 +375,13 @@ int bca_commit_kv(const bca_dims* d, const void* k_blk, const void* v_blk, void*
              : BCA_ERR_CUDA;
 }
 
-int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* v_blk,
-               void* k_pool, void* v_pool, const int32_t* page_table, const int32_t* prefix_len,
-               void* out, int commit, void* ws, size_t ws_bytes, bca_stream_t stream) {
+namespace {
+// Decode step (causal = 0) or short causal extend (causal = 1): the same
+// kernels, the extend with one-token mask blocks and no prefix alignment.
+int decode_impl(const bca_dims* d, const void* q, const void* k_blk, const void* v_blk,
+                void* k_pool, void* v_pool, const int32_t* page_table,
+                const int32_t* prefix_len, void* out, int commit, int causal, void* ws,
+                size_t ws_bytes, bca_stream_t stream) {
   int rc = validate_dims(d);
   if (rc) return rc;
   if (commit != 0 && commit != 1) return BCA_ERR_INVALID_ARG;
@@ -402,6 +406,7 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
 
   AttnParams p = base_params(d);
   p.mode = kModeDecode;
+  p.causal = causal;
   p.hpr = p.G;
   p.tpm = 128 / p.G;
   p.n_hp = 1;
@@ -454,6 +459,21 @@ int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* 
       return BCA_ERR_CUDA;
   }
   return BCA_OK;
+}
+}  // namespace
+
+int bca_decode(const bca_dims* d, const void* q, const void* k_blk, const void* v_blk,
+               void* k_pool, void* v_pool, const int32_t* page_table, const int32_t* prefix_len,
+               void* out, int commit, void* ws, size_t ws_bytes, bca_stream_t stream) {
+  return decode_impl(d, q, k_blk, v_blk, k_pool, v_pool, page_table, prefix_len, out, commit, 0,
+                     ws, ws_bytes, stream);
+}
+
+int bca_extend(const bca_dims* d, const void* q, const void* k_new, const void* v_new,
+               void* k_pool, void* v_pool, const int32_t* page_table, const int32_t* prefix_len,
+               void* out, int commit, void* ws, size_t ws_bytes, bca_stream_t stream) {
+  return decode_impl(d, q, k_new, v_new, k_pool, v_pool, page_table, prefix_len, out, commit, 1,
+                     ws, ws_bytes, stream);
 }
 
 int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,

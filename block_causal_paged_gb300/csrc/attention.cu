@@ -342,7 +342,7 @@ struct Planner {
       nt[k] = 0;  // no sequence
       if (b < B) {
         int v = __ldg(p.lens + b);
-        if (v < 0 || v % D != 0 || (long long)v + D > (long long)p.max_pages * p.S) {
+        if (v < 0 || (!p.causal && v % D != 0) || (long long)v + D > (long long)p.max_pages * p.S) {
           bad = 1;  // treated as an empty prefix, reported in the status word
           v = 0;
         }
@@ -461,7 +461,8 @@ struct Planner {
       qbase[m] = P + tok;
     }
     const int n_m = ntok[1] > 0 ? 2 : 1;
-    emit_item(t1 - t0, n_m, 0, qtok, qhead, ntok, qbase, P, D, split);
+    // mask block: the D tokens form one block, or one block each (causal)
+    emit_item(t1 - t0, n_m, 0, qtok, qhead, ntok, qbase, P, p.causal ? 1 : D, split);
     const int n_pre = ceil_div(P, kTileKeys);
     // prefix tiles through the page table
     if (t0 < n_pre) emit_pool_tiles_contig(b, g, P, t0, min(t1, n_pre));
@@ -469,7 +470,7 @@ struct Planner {
     for (int t = max(t0, n_pre); t < t1 && ok; ++t) {
       const int o = (t - n_pre) * kTileKeys;
       const int nvalid = min(kTileKeys, D - o);
-      emit_dense_tile(g, b * D + o, nvalid, 0, P + o, nvalid == kTileKeys);
+      emit_dense_tile(g, b * D + o, nvalid, 0, P + o, !p.causal && nvalid == kTileKeys);
     }
   }
 

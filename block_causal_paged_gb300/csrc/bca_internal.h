@@ -58,6 +58,8 @@ struct AttnParams {
   int n_rb;            // decode: row blocks per KV head (each = 2 M-tiles)
   int ch_min, waves;   // decode split policy
   int fused_plan;      // decode: every CTA plans for itself (batch <= kFusedPlanMax)
+  int causal;          // decode: the D query tokens attend each other causally (short
+                       // extend; the prefix length then need not be a multiple of D)
   int n_qt_max;        // prefill: query tiles of the longest sequence (host bound)
   int n_rb_max;        // multicanvas: row blocks of the longest live list (host bound)
   float scale_log2;    // softmax scale * log2(e)

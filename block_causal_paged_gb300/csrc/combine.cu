@@ -63,7 +63,8 @@ __device__ __forceinline__ void commit_rows(const AttnParams& p, int first_cta) 
   for (long long row = warp; row < rows; row += n_warps) {
     const int b = (int)(row / p.Dblk), t = (int)(row % p.Dblk);
     const int P = __ldg(p.lens + b);
-    if (P < 0 || P % p.Dblk != 0 || (long long)P + p.Dblk > (long long)p.max_pages * p.S)
+    if (P < 0 || (!p.causal && P % p.Dblk != 0) ||
+        (long long)P + p.Dblk > (long long)p.max_pages * p.S)
       continue;  // a bad prefix length is reported by the plan kernel
     const int pos = P + t;
     const int page = __ldg(p.page_table + (size_t)b * p.max_pages + pos / p.S);

@@ -39,7 +39,8 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 __device__ __forceinline__ int plan_prefix(const AttnParams& p, int b, int* bad) {
   const int P = __ldg(p.lens + b);
-  if (P < 0 || P % p.Dblk != 0 || (long long)P + p.Dblk > (long long)p.max_pages * p.S) {
+  if (P < 0 || (!p.causal && P % p.Dblk != 0) ||
+      (long long)P + p.Dblk > (long long)p.max_pages * p.S) {
     *bad = 1;
     return 0;  // treated as an empty prefix, reported in the status word
   }

@@ -160,6 +160,32 @@ int bca_decode(const bca_dims* dims, const void* q, const void* k_blk, const voi
                size_t workspace_bytes, bca_stream_t stream);
 
 /*
+ * bca_extend -- a short causal extend over the paged cache.
+ *
+ * "Introspective Diffusion Language Model", "3.3 I-DLM Serving Stack" and
+ * Appendix D: introspective decoding appends 2N-1 causal query tokens per
+ * step (at most 9 for the short extends served by one paged attention
+ * kernel instead of ragged attention + paged attention + merge).  The
+ * dims' block_size is the number of new tokens n.  Query i of sequence b
+ * (position P_b + i, P_b = prefix_len[b]) attends every key of the prefix
+ * 0 .. P_b-1, read through the page table, and the new keys 0 .. i
+ * (k_new/v_new): the block rule with one-token blocks.  P_b may be any
+ * length with P_b + n <= max_pages_per_seq * S.  Any n >= 1 works; the
+ * kernels are the decode step's.
+ *
+ * commit = 1 also copies the n new K/V rows into positions [P_b, P_b+n) of
+ * the pools in the same call (the attention never reads those slots).
+ *
+ * q, out: [B, n, Hq, d] bf16.  k_new, v_new: [B, n, Hkv, d] bf16.  Other
+ * arguments, the workspace (BCA_OP_DECODE sizes) and the errors as for
+ * bca_decode.
+ */
+int bca_extend(const bca_dims* dims, const void* q, const void* k_new, const void* v_new,
+               void* k_pool, void* v_pool, const int32_t* page_table,
+               const int32_t* prefix_len, void* out, int commit, void* workspace,
+               size_t workspace_bytes, bca_stream_t stream);
+
+/*
  * bca_confidence -- the top prediction at each position and its probability.
  *
  * "Inference: Fewer, smaller forwards", "Advancement 2: tau_conf": on every

@@ -42,10 +42,11 @@ class DecodeRun:
         self.d = dims_for_decode(case)
         self.ws = bca.new_workspace(self.d, bca.OP_DECODE, device=dev)
 
-    def run(self, commit=False, ws=None):
+    def run(self, commit=False, ws=None, extend=False):
         ws = self.ws if ws is None else ws
-        bca.bca_decode(self.d, self.q, self.k_blk, self.v_blk, self.k_pool, self.v_pool,
-                       self.page_table, self.prefix_len, self.out, commit, ws)
+        fn = bca.bca_extend if extend else bca.bca_decode
+        fn(self.d, self.q, self.k_blk, self.v_blk, self.k_pool, self.v_pool, self.page_table,
+           self.prefix_len, self.out, commit, ws)
         torch.cuda.synchronize()
         return self.out
 
