@@ -329,6 +329,49 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return rounded.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def qkv_post(qkv, positions, Hq: int, Hkv: int, q_norm_w=None, k_norm_w=None,
+             eps: float = 1e-6, rope_theta: float = 0.0):
+    """The step between the QKV projection and attention, in fp64.
+
+    "Inference: Fewer, smaller forwards", "Advancement 16" (an optional fused
+    QKV-post: RoPE, norms and the arena write) and "Advancement 10" (RoPE is
+    baked into keys at the token's true absolute position).  qkv
+    [..., Hq + 2 Hkv, d]: the projection's output, query heads first, then
+    key heads, then value heads; positions [...] the absolute positions.
+    Norms: each query and key head vector x is RMS-normalised with a weight
+    w of length d shared by the heads, x * w / sqrt(mean(x^2) + eps) (no
+    norm where the weight is None).  RoPE (rope_theta > 0): the pair
+    (x_i, x_{i+d/2}), i < d/2, is rotated by the angle pos * theta^(-2i/d).
+    Values pass through.  Returns fp64 (q [..., Hq, d], k [..., Hkv, d],
+    v [..., Hkv, d]); rounding to bf16 is the caller's (``bf16_round``).
+    """
+    x = _f64(qkv)
+    d = x.shape[-1]
+    q = x[..., :Hq, :].copy()
+    k = x[..., Hq:Hq + Hkv, :].copy()
+    v = x[..., Hq + Hkv:Hq + 2 * Hkv, :].copy()
+
+    def rms(a, w):
+        if w is None:
+            return a
+        w = _f64(w)
+        return a * w / np.sqrt(np.mean(a * a, axis=-1, keepdims=True) + eps)
+
+    q, k = rms(q, q_norm_w), rms(k, k_norm_w)
+    if rope_theta > 0:
+        half = d // 2
+        inv_freq = rope_theta ** (-2.0 * np.arange(half, dtype=np.float64) / d)
+        ang = _i64(positions).astype(np.float64)[..., None] * inv_freq  # [..., d/2]
+        c, s = np.cos(ang)[..., None, :], np.sin(ang)[..., None, :]
+
+        def rot(a):
+            a1, a2 = a[..., :half], a[..., half:]
+            return np.concatenate([a1 * c - a2 * s, a2 * c + a1 * s], axis=-1)
+
+        q, k = rot(q), rot(k)
+    return q, k, v
+
+
 def confidence(logits):
     """Top prediction and its probability for each row of logits.
 
