@@ -281,8 +281,8 @@ def time_steps(torch, fn, steps, stream):
 
 
 def other_rows(args, bca, workloads, torch, pk, dev, stream):
-    """The block-causal prefill (4 x 8192), the short causal extend (batch 64,
-    9 tokens) and the multicanvas step (batch 16, prompt 1024, 3 canvases of
+    """The block-causal prefill (4 x 8192), the QKV-post of a decode step's
+    blocks, the short causal extend (batch 64, 9 tokens) and the multicanvas step (batch 16, prompt 1024, 3 canvases of
     256; and 5 canvases under a 1024-token sliding window), each timed over repeated calls with CUDA events and set against
     its roofline: algorithmic flops (every visible (query, key) pair costs 4d
     per query head) and bytes (every input byte once, the output, page
@@ -349,6 +349,34 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         nl = int(case.live_count.sum())
         bytes2 = (A + nl) * case.Hkv * case.d * 2 * 2.0 + 2 * nl * case.Hq * case.d * 2.0
         res[name] = dict(roof(flops2, bytes2, ms2), workload=desc)
+
+    # QKV-post: batch 64 blocks of 64 tokens after the serving prefixes,
+    # 32/8 heads, d = 128, norms + RoPE, the key / value rows written to pages
+    Pq = workloads.prefix_loguniform_blocks(64, 128, 32768, 64, seed=args.seed)
+    cq = workloads.make_qkv_post_case(64, 64, 32, 8, 128, prefix_len=Pq, seed=args.seed)
+    dq = bca.dims(cq.B, cq.n, cq.Hq, cq.Hkv, cq.d, cq.pool.page_size, cq.pool.num_pages,
+                  cq.pool.max_pages_per_seq)
+    tq = {k_: v_.to(dev) for k_, v_ in (("qkv", cq.qkv), ("pos", cq.positions),
+                                        ("qw", cq.q_norm_w), ("kw", cq.k_norm_w),
+                                        ("wp", cq.write_pos), ("kp", cq.pool.k_pool),
+                                        ("vp", cq.pool.v_pool), ("pt", cq.pool.page_table))}
+    oq = torch.empty((cq.B, cq.n, cq.Hq, cq.d), dtype=torch.bfloat16, device=dev)
+    ok_ = torch.empty((cq.B, cq.n, cq.Hkv, cq.d), dtype=torch.bfloat16, device=dev)
+    ov = torch.empty_like(ok_)
+    wq = bca.new_workspace(dq, bca.OP_COMMIT, device=dev)
+    ms_q = time_calls(lambda: bca.bca_qkv_post(dq, tq["qkv"], tq["pos"], oq, ok_, ov, wq,
+                                               q_norm_w=tq["qw"], k_norm_w=tq["kw"], eps=1e-6,
+                                               rope_theta=1e6, write_pos=tq["wp"],
+                                               k_pool=tq["kp"], v_pool=tq["vp"],
+                                               page_table=tq["pt"]), 50)
+    tokens = cq.B * cq.n
+    row = (cq.Hq + 2 * cq.Hkv) * cq.d * 2.0
+    bytes_q = tokens * (2 * row + 2 * cq.Hkv * cq.d * 2.0 + 8.0) + 2 * cq.d * 2.0
+    res["qkv_post"] = dict(roof(0.0, bytes_q, ms_q),
+                           workload="batch 64 x 64 tokens after the serving prefixes, 32/8 heads, "
+                                    "d=128: per-head RMS norms + RoPE (theta 1e6) of q and k, "
+                                    "K/V rows written to pages of 16")
+    del tq, oq, ok_, ov, wq, cq
 
     # short causal extend: batch 64, 9 new tokens (2N-1, N = 5), prefixes at
     # token granularity, 32/8 heads, d = 128, the new rows committed

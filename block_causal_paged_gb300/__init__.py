@@ -47,10 +47,10 @@ class Dims(ctypes.Structure):
 
 class KernelTimes(ctypes.Structure):
     """struct bca_kernel_times."""
-    _fields_ = [("launches", _i32 * 6), ("total_ms", ctypes.c_double * 6)]
+    _fields_ = [("launches", _i32 * 7), ("total_ms", ctypes.c_double * 7)]
 
 
-KERNEL_NAMES = ("attention", "combine", "commit", "promote", "plan", "confidence")
+KERNEL_NAMES = ("attention", "combine", "commit", "promote", "plan", "confidence", "qkv_post")
 
 _DP = ctypes.POINTER(Dims)
 SIGNATURES = {
@@ -64,6 +64,8 @@ SIGNATURES = {
                    ctypes.c_int),
     "bca_extend": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _sz, _vp],
                    ctypes.c_int),
+    "bca_qkv_post": ([_DP, _vp, _vp, _vp, _vp, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                      _vp, _sz, _vp], ctypes.c_int),
     "bca_commit_kv": ([_DP, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp], ctypes.c_int),
     "bca_prefill": ([_DP, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
                     ctypes.c_int),
@@ -185,6 +187,18 @@ def bca_extend(d: Dims, q, k_new, v_new, k_pool, v_pool, page_table, prefix_len,
                            _ptr(v_pool), _ptr(page_table), _ptr(prefix_len), _ptr(out),
                            1 if commit else 0, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "bca_extend")
+
+
+def bca_qkv_post(d: Dims, qkv, positions, q_out, k_out, v_out, workspace, q_norm_w=None,
+                 k_norm_w=None, eps: float = 1e-6, rope_theta: float = 0.0, write_pos=None,
+                 k_pool=None, v_pool=None, page_table=None, kv_pos=None, stream=None) -> None:
+    """Norms + RoPE of the QKV projection's output, optional cache write (see include/bca.h)."""
+    rc = load().bca_qkv_post(ctypes.byref(d), _ptr(qkv), _ptr(positions), _ptr(q_norm_w),
+                             _ptr(k_norm_w), float(eps), float(rope_theta), _ptr(q_out),
+                             _ptr(k_out), _ptr(v_out), _ptr(write_pos), _ptr(k_pool),
+                             _ptr(v_pool), _ptr(page_table), _ptr(kv_pos), _ptr(workspace),
+                             workspace.numel(), _stream(stream))
+    _check(rc, "bca_qkv_post")
 
 
 def bca_decode_static_scratch(d: Dims, q, k_blk, v_blk, k_pool, v_pool, page_table, prefix_len,

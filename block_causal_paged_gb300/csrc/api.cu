@@ -317,6 +317,65 @@ int bca_read_tile_counters(void* ws, int64_t counters[3], bca_stream_t stream) {
   return BCA_OK;
 }
 
+int bca_qkv_post(const bca_dims* d, const void* qkv, const int32_t* positions,
+                 const void* q_norm_w, const void* k_norm_w, float eps, float rope_theta,
+                 void* q_out, void* k_out, void* v_out, const int32_t* write_pos,
+                 void* k_pool, void* v_pool, const int32_t* page_table, int32_t* kv_pos,
+                 void* ws, size_t ws_bytes, bca_stream_t stream) {
+  int rc = validate_dims(d);
+  if (rc) return rc;
+  if (!(eps >= 0.f) || !std::isfinite(eps) || !(rope_theta >= 0.f) || !std::isfinite(rope_theta))
+    return BCA_ERR_INVALID_ARG;
+  if (d->batch == 0) return BCA_OK;
+  if (!qkv || !q_out || !k_out || !v_out || !ws) return BCA_ERR_NULL;
+  if ((rope_theta > 0.f || kv_pos) && !positions) return BCA_ERR_NULL;
+  if (write_pos && (!k_pool || !v_pool || !page_table)) return BCA_ERR_NULL;
+  if (kv_pos && !write_pos) return BCA_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out) ||
+      (write_pos && (!aligned16(k_pool) || !aligned16(v_pool))) || !aligned16(ws))
+    return BCA_ERR_ALIGN;
+  if (ws_bytes < kWsHeaderBytes) return BCA_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((rc = device_info(&di))) return rc;
+  QkvPostParams c;
+  std::memset(&c, 0, sizeof(c));
+  c.qkv = (const uint16_t*)qkv;
+  c.positions = positions;
+  c.q_norm_w = (const uint16_t*)q_norm_w;
+  c.k_norm_w = (const uint16_t*)k_norm_w;
+  c.eps = eps;
+  c.rope_theta = rope_theta;
+  if (rope_theta > 0.f) {
+    const int half = d->head_dim / 2;
+    for (int i = 0; i < half; ++i) {
+      const double f = std::pow((double)rope_theta, -2.0 * i / d->head_dim);  // radians per position
+      const double t = f / 6.283185307179586476925286766559;                 // turns per position
+      c.rope_turns[i] = (unsigned long long)(t * 18446744073709551616.0);     // * 2^64, < 2^62
+    }
+  }
+  c.q_out = (uint16_t*)q_out;
+  c.k_out = (uint16_t*)k_out;
+  c.v_out = (uint16_t*)v_out;
+  c.write_pos = write_pos;
+  c.k_pool = (uint16_t*)k_pool;
+  c.v_pool = (uint16_t*)v_pool;
+  c.page_table = page_table;
+  c.kv_pos = kv_pos;
+  c.B = d->batch;
+  c.n = d->block_size;
+  c.Hq = d->num_q_heads;
+  c.Hkv = d->num_kv_heads;
+  c.S = d->page_size;
+  c.num_pages = d->num_pages;
+  c.max_pages = d->max_pages_per_seq;
+  c.hdr = (WsHeader*)ws;
+  cudaStream_t s = (cudaStream_t)stream;
+  return timed(BCA_KERNEL_QKV_POST, s, [&] { return launch_qkv_post(c, d->head_dim, di.sms, s); }) ==
+                 cudaSuccess
+             ? BCA_OK
+             : BCA_ERR_CUDA;
+}
+
 int bca_confidence(int64_t rows, int64_t vocab, int64_t ld, int dtype, const void* logits,
                    int32_t* argmax, float* conf, bca_stream_t stream) {
   if (rows < 0 || vocab < 1 || vocab >= (1ll << 31) || ld < vocab) return BCA_ERR_INVALID_ARG;

@@ -141,6 +141,29 @@ struct CommitParams {
 };
 cudaError_t launch_commit(const CommitParams& c, cudaStream_t stream);
 
+// QKV-post: norms + RoPE of the projection's output, optional cache write.
+struct QkvPostParams {
+  const uint16_t* qkv;        // [B * n, Hq + 2 Hkv, d]
+  const int32_t* positions;   // [B * n] (may be null without RoPE / kv_pos)
+  const uint16_t* q_norm_w;   // [d] or null
+  const uint16_t* k_norm_w;   // [d] or null
+  float eps, rope_theta;      // rope_theta 0: no rotation
+  // RoPE frequency of pair i (< d/2) in turns per position, as a 64-bit
+  // fixed-point fraction: round(theta^(-2i/d) / (2 pi) * 2^64)
+  unsigned long long rope_turns[64];
+  uint16_t* q_out;            // [B * n, Hq, d]
+  uint16_t* k_out;            // [B * n, Hkv, d]
+  uint16_t* v_out;
+  const int32_t* write_pos;   // [B * n] cache position, -1 = none; null: no cache write
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  const int32_t* page_table;
+  int32_t* kv_pos;            // [num_pages, S] or null
+  int B, n, Hq, Hkv, S, num_pages, max_pages;
+  WsHeader* hdr;
+};
+cudaError_t launch_qkv_post(const QkvPostParams& c, int head_dim, int n_sms, cudaStream_t stream);
+
 // Arena promotion after a multicanvas step.
 struct PromoteParams {
   const uint16_t* k_live;

@@ -186,6 +186,42 @@ int bca_extend(const bca_dims* dims, const void* q, const void* k_new, const voi
                size_t workspace_bytes, bca_stream_t stream);
 
 /*
+ * bca_qkv_post -- norms, RoPE and the cache write after the QKV projection.
+ *
+ * "Inference: Fewer, smaller forwards", "Advancement 16" (an optional fused
+ * QKV-post: RoPE, norms, arena write) and "Advancement 10" (RoPE is baked
+ * into the keys at each token's true absolute position).  The dims' batch B
+ * and block_size n give B * n tokens (a block per sequence, or the live rows
+ * of a multicanvas step).  For each token:
+ *   q, k: every head vector x becomes x * w / sqrt(mean(x^2) + eps), w of
+ *         length d shared by the heads (q_norm_w / k_norm_w; NULL: no norm),
+ *         then each pair (x_i, x_{i+d/2}), i < d/2, is rotated by the angle
+ *         positions[t] * rope_theta^(-2i/d) (rope_theta = 0: no rotation);
+ *   v:    copied bit for bit.
+ * Computed in fp32 with one rounding to bf16 (nearest even) per output.
+ * If write_pos is not NULL, a token with write_pos[t] >= 0 also has its
+ * finished key and value rows written to cache position write_pos[t] of its
+ * sequence (page page_table[b][p / S], slot p % S) and, if kv_pos is not
+ * NULL, its position stored in kv_pos[page][slot] (arena mode).  The
+ * outputs feed bca_decode / bca_extend (k_blk, v_blk) or bca_multicanvas
+ * (the live rows).
+ *
+ * qkv: bf16 [B, n, Hq + 2 Hkv, d] (query heads, then key heads, then value
+ * heads).  positions, write_pos: int32 [B, n] (positions may be NULL when
+ * rope_theta = 0 and kv_pos is NULL).  q_norm_w, k_norm_w: bf16 [d] or
+ * NULL.  q_out: bf16 [B, n, Hq, d]; k_out, v_out: bf16 [B, n, Hkv, d].
+ * eps >= 0, rope_theta >= 0.  Workspace: the header (BCA_OP_COMMIT size),
+ * for the status word: a write position past the page table is reported as
+ * BCA_ERR_DEVICE_BAD_LENGTH, a page id outside the pool as
+ * BCA_ERR_DEVICE_PAGE_OOB, and that write is skipped.
+ */
+int bca_qkv_post(const bca_dims* dims, const void* qkv, const int32_t* positions,
+                 const void* q_norm_w, const void* k_norm_w, float eps, float rope_theta,
+                 void* q_out, void* k_out, void* v_out, const int32_t* write_pos,
+                 void* k_pool, void* v_pool, const int32_t* page_table, int32_t* kv_pos,
+                 void* workspace, size_t workspace_bytes, bca_stream_t stream);
+
+/*
  * bca_confidence -- the top prediction at each position and its probability.
  *
  * "Inference: Fewer, smaller forwards", "Advancement 2: tau_conf": on every
@@ -363,7 +399,8 @@ int bca_decode_static_scratch(const bca_dims* dims, const void* q, const void* k
 #define BCA_KERNEL_PROMOTE 3   /* multicanvas arena promotion */
 #define BCA_KERNEL_PLAN 4      /* work planning (prefill, multicanvas, decode batches > 64) */
 #define BCA_KERNEL_CONFIDENCE 5 /* softmax-plus-argmax over the vocabulary */
-#define BCA_KERNEL_KINDS 6
+#define BCA_KERNEL_QKV_POST 6  /* norms + RoPE + cache write after the QKV projection */
+#define BCA_KERNEL_KINDS 7
 
 typedef struct bca_kernel_times {
   int32_t launches[BCA_KERNEL_KINDS];

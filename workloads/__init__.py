@@ -405,3 +405,49 @@ def confidence_logits(rows: int, vocab: int, seed: int = 0, dtype=None, device="
         lift = 6.0 + 8.0 * torch.rand((len(peaked),), generator=g, device=device)
         x[peaked, tok] += lift
     return x.to(dtype)
+
+
+# ---------------------------------------------------------------------------
+# QKV-post (the step between the QKV projection and attention)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class QkvPostCase:
+    B: int
+    n: int
+    Hq: int
+    Hkv: int
+    d: int
+    qkv: torch.Tensor             # [B, n, Hq + 2 Hkv, d] bf16
+    positions: torch.Tensor       # int32 [B, n]
+    q_norm_w: torch.Tensor        # bf16 [d]
+    k_norm_w: torch.Tensor
+    write_pos: torch.Tensor       # int32 [B, n]: cache position of each token
+    pool: PagedPool
+    seed: int
+
+
+def make_qkv_post_case(B: int, n: int, Hq: int, Hkv: int, d: int, prefix_len=None,
+                       page_size: int = 16, seed: int = 0, qkv_scale: float = 2.0,
+                       pos_max: int = 32768) -> QkvPostCase:
+    """Projection rows N(0, qkv_scale^2) in bf16, norm weights 1 + N(0, 0.1^2)
+    (learned weights near one), and positions: the block after each prefix
+    (P_b .. P_b+n-1, also the cache positions) when ``prefix_len`` is given,
+    else distinct random positions below ``pos_max`` written to the first n
+    cache slots (an arena)."""
+    g = _gen(seed, 401)
+    qkv = (torch.randn((B, n, Hq + 2 * Hkv, d), generator=g) * qkv_scale).to(torch.bfloat16)
+    q_norm_w = (1.0 + 0.1 * torch.randn((d,), generator=g)).to(torch.bfloat16)
+    k_norm_w = (1.0 + 0.1 * torch.randn((d,), generator=g)).to(torch.bfloat16)
+    if prefix_len is not None:
+        P = torch.tensor(prefix_len, dtype=torch.int64)
+        positions = (P[:, None] + torch.arange(n)[None, :]).to(torch.int32)
+        write_pos = positions.clone()
+        cap = [int(p) + n for p in prefix_len]
+    else:
+        positions = torch.stack([torch.randperm(pos_max, generator=g)[:n] for _ in range(B)])
+        positions = positions.to(torch.int32)
+        write_pos = torch.arange(n, dtype=torch.int32)[None, :].repeat(B, 1)
+        cap = [n] * B
+    pool = build_paged_pool(cap, Hkv, d, page_size, seed, fill_bits_value=None)
+    return QkvPostCase(B, n, Hq, Hkv, d, qkv, positions, q_norm_w, k_norm_w, write_pos, pool, seed)
