@@ -15,12 +15,12 @@
 // cache at write_pos (page page_table[b][p / S], slot p % S), with the
 // token's position stored in kv_pos (arena mode).
 //
-// A warp per group of 8 heads of a token, a half-warp per head: each lane
+// A warp per group of 4 heads of a token, a half-warp per head: each lane
 // holds d/32 consecutive elements and their rotation partners d/2 further, so
 // a rotation needs no shuffle and every load of a head pair is contiguous.
 // The group's loads are issued one token ahead of the processing (software
-// pipeline), and the grid is what stays resident.  Arithmetic in fp32, one rounding to
-// bf16 at the end.  The angle needs no floating point on a large argument:
+// pipeline), and the grid is what stays resident.  Arithmetic in fp32, one
+// rounding to bf16 at the end.  The angle needs no floating point on a large argument:
 // the host gives each pair's frequency in turns per position as a 64-bit
 // fixed-point fraction F, and pos * F modulo 2^64 (integer arithmetic, exact
 // for any int32 position) is the angle's fraction of a turn; its top 32 bits,
@@ -49,9 +49,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Warp w of W = n_grp * W_t warps takes head group g = w % n_grp (heads
-// 8g .. 8g+7) of tokens w / n_grp, + W_t, ...: the group, its heads' kinds and
+// 4g .. 4g+3) of tokens w / n_grp, + W_t, ...: the group, its heads' kinds and
 // output offsets are fixed for the warp's life.  Each half-warp takes one head
-// of a pair (heads 8g + 2p + s for half s): lane j of the half holds elements
+// of a pair (heads 4g + 2p + s for half s): lane j of the half holds elements
 // kV*j .. kV*j+kV-1 and their rotation partners d/2 further (kV = d/32), so a
 // head's sum of squares takes four shuffle rounds shared by the pair.
 template <int HD>

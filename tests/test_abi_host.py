@@ -161,3 +161,29 @@ def test_confidence_argument_errors(bca):
     assert f(4, 8, 8, 0, base + 1, base, base, None) == bca.ERR_ALIGN        # bf16 logits at an odd byte
     assert f(4, 8, 8, 1, base + 2, base, base, None) == bca.ERR_ALIGN        # fp32 logits at 2 bytes
     assert f(4, 8, 8, 0, base, base + 2, base, None) == bca.ERR_ALIGN        # int32 argmax misaligned
+
+
+def test_extend_and_qkv_post_argument_errors(bca):
+    """Host checks of bca_extend and bca_qkv_post that need no GPU."""
+    lib = bca.load()
+    buf = (ctypes.c_uint8 * 4096)()
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    d = _d(bca, block_size=9)
+    assert lib.bca_extend(ctypes.byref(d), a, a, a, a, a, a, a, a, 2, a, 1 << 20, None) == \
+        bca.ERR_INVALID_ARG                                   # commit flag not 0/1
+    assert lib.bca_extend(ctypes.byref(d), a, a, a, a, a, a, None, a, 0, a, 1 << 20, None) == \
+        bca.ERR_NULL
+    f = lib.bca_qkv_post
+    ok = (a, a, None, None, 1e-6, 0.0, a, a, a, None, None, None, None, None, a, 256, None)
+    assert f(ctypes.byref(d), *ok[:4], -1.0, *ok[5:]) == bca.ERR_INVALID_ARG   # eps < 0
+    assert f(ctypes.byref(d), *ok[:5], -2.0, *ok[6:]) == bca.ERR_INVALID_ARG   # theta < 0
+    assert f(ctypes.byref(d), a, None, None, None, 1e-6, 1e4, a, a, a, None, None, None, None,
+             None, a, 256, None) == bca.ERR_NULL                               # RoPE needs positions
+    assert f(ctypes.byref(d), a, a, None, None, 1e-6, 0.0, a, a, a, a, None, None, None, None,
+             a, 256, None) == bca.ERR_NULL                                     # write without pools
+    assert f(ctypes.byref(d), a, a, None, None, 1e-6, 0.0, a, a, a, None, None, None, None, a,
+             a, 256, None) == bca.ERR_INVALID_ARG                              # kv_pos without write
+    assert f(ctypes.byref(d), a + 2, *ok[1:]) == bca.ERR_ALIGN
+    assert f(ctypes.byref(d), *ok[:14], a, 16, None) == bca.ERR_WORKSPACE
+    z = _d(bca, batch=0)
+    assert f(ctypes.byref(z), *ok) == bca.OK                                   # empty batch: no-op
