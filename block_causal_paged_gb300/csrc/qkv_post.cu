@@ -27,6 +27,7 @@
 // read as a signed number, map to [-pi, pi) for the single-precision sine and
 // cosine (a phase accumulator).  Its error is that of F, about 2^-22 turns
 // at the largest positions.
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 
@@ -239,17 +240,21 @@ cudaError_t launch_qkv_post(const QkvPostParams& c, int head_dim, int n_sms, cud
   const int n_grp = (c.Hq + 2 * c.Hkv + kUnroll - 1) / kUnroll;
   // warps: a whole number of groups, at most what is resident at once (each
   // warp loops over tokens), at most one per unit
-  static int resident[2] = {0, 0};  // blocks per SM, per head dim (a fixed property of the kernel)
+  // blocks per SM, per head dim: a fixed property of the kernel, queried once
+  // (host threads that race here store the same value)
+  static std::atomic<int> resident[2] = {{0}, {0}};
   const int hi = head_dim == 128 ? 1 : 0;
-  if (resident[hi] == 0) {
+  int per_sm = resident[hi].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
     int nb = 0;
     const cudaError_t e = head_dim == 128
         ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, qkv_post_kernel<128>, kThreadsQP, 0)
         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, qkv_post_kernel<64>, kThreadsQP, 0);
     if (e != cudaSuccess) return e;
-    resident[hi] = nb > 0 ? nb : 1;
+    per_sm = nb > 0 ? nb : 1;
+    resident[hi].store(per_sm, std::memory_order_relaxed);
   }
-  long long W = (long long)(n_sms > 0 ? n_sms : 1) * resident[hi] * (kThreadsQP / 32);
+  long long W = (long long)(n_sms > 0 ? n_sms : 1) * per_sm * (kThreadsQP / 32);
   if (W > T * n_grp) W = T * n_grp;
   W = W / n_grp * n_grp;
   if (W < n_grp) W = n_grp;
