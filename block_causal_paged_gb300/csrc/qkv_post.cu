@@ -83,18 +83,26 @@ __global__ void __launch_bounds__(kThreadsQP) qkv_post_kernel(const __grid_const
     kd[p] = h < c.Hq ? 0 : (h < c.Hq + c.Hkv ? 1 : 2);
     gh[p] = kd[p] == 0 ? h : (kd[p] == 1 ? h - c.Hq : h - c.Hq - c.Hkv);
   }
-  // this lane's elements i = kV*jl + e and i + d/2: norm weights, RoPE turns
-  float wq[2 * kV], wk[2 * kV];
+  // this lane's elements i = kV*jl + e and i + d/2: the norm weight of each
+  // of its heads (fixed for the warp's life) and the RoPE turns
+  float wsel[kPairs][2 * kV];
+  bool normed[kPairs];
   unsigned long long turns[kV];
 #pragma unroll
-  for (int e = 0; e < kV; ++e) {
-    const int i = kV * jl + e;
-    wq[e] = has_qw ? bf2f(__ldg(c.q_norm_w + i)) : 1.f;
-    wq[kV + e] = has_qw ? bf2f(__ldg(c.q_norm_w + i + kHalf)) : 1.f;
-    wk[e] = has_kw ? bf2f(__ldg(c.k_norm_w + i)) : 1.f;
-    wk[kV + e] = has_kw ? bf2f(__ldg(c.k_norm_w + i + kHalf)) : 1.f;
-    turns[e] = c.rope_turns[i];
+  for (int p = 0; p < kPairs; ++p) {
+    const uint16_t* wv = kd[p] == 0 ? c.q_norm_w : (kd[p] == 1 ? c.k_norm_w : nullptr);
+    normed[p] = wv != nullptr;
+#pragma unroll
+    for (int e = 0; e < kV; ++e) {
+      const int i = kV * jl + e;
+      wsel[p][e] = wv ? bf2f(__ldg(wv + i)) : 1.f;
+      wsel[p][kV + e] = wv ? bf2f(__ldg(wv + i + kHalf)) : 1.f;
+    }
   }
+#pragma unroll
+  for (int e = 0; e < kV; ++e) turns[e] = c.rope_turns[kV * jl + e];
+  // a group of value heads only is a copy
+  const bool all_v = h0 >= c.Hq + c.Hkv;
   const float kTurnToRad = 6.28318530717958647692f / 4294967296.0f;  // 2 pi / 2^32
   auto load_tok = [&](int tkn, Vec (&raw)[kPairs][2], int& pos, int& wp) {
     const uint16_t* src = c.qkv + ((size_t)tkn * Htot + h0 + sub) * HD + kV * jl;
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(kThreadsQP) qkv_post_kernel(const __grid_const
       unpack(raw[p][0], &y[p][0]);
       unpack(raw[p][1], &y[p][kV]);
     }
-    if (has_qw || has_kw) {
+    if (!all_v && (has_qw || has_kw)) {
       float ss[kPairs];
 #pragma unroll
       for (int p = 0; p < kPairs; ++p) {
@@ -178,13 +186,12 @@ __global__ void __launch_bounds__(kThreadsQP) qkv_post_kernel(const __grid_const
       }
 #pragma unroll
       for (int p = 0; p < kPairs; ++p) {
-        const bool normed = kd[p] == 0 ? has_qw : (kd[p] == 1 && has_kw);
-        const float r = normed ? rsqrtf(ss[p] * (1.0f / HD) + c.eps) : 1.f;
+        const float r = normed[p] ? rsqrtf(ss[p] * (1.0f / HD) + c.eps) : 1.f;
 #pragma unroll
-        for (int e = 0; e < 2 * kV; ++e) y[p][e] *= r * (kd[p] == 0 ? wq[e] : wk[e]);
+        for (int e = 0; e < 2 * kV; ++e) y[p][e] *= r * wsel[p][e];
       }
     }
-    if (c.rope_theta > 0.f) {
+    if (!all_v && c.rope_theta > 0.f) {
 #pragma unroll
       for (int p = 0; p < kPairs; ++p) {
 #pragma unroll
@@ -201,17 +208,15 @@ __global__ void __launch_bounds__(kThreadsQP) qkv_post_kernel(const __grid_const
 #pragma unroll
     for (int p = 0; p < kPairs; ++p) {
       if (!live[p]) continue;
-      Vec o0, o1;
-      if constexpr (kV == 4) {
-        o0 = make_uint2(pack_bf16x2(y[p][0], y[p][1]), pack_bf16x2(y[p][2], y[p][3]));
-        o1 = make_uint2(pack_bf16x2(y[p][4], y[p][5]), pack_bf16x2(y[p][6], y[p][7]));
-      } else {
-        o0 = pack_bf16x2(y[p][0], y[p][1]);
-        o1 = pack_bf16x2(y[p][2], y[p][3]);
-      }
-      if (kd[p] == 2) {  // values pass through as bits
-        o0 = raw[p][0];
-        o1 = raw[p][1];
+      Vec o0 = raw[p][0], o1 = raw[p][1];  // values pass through as bits
+      if (kd[p] != 2) {
+        if constexpr (kV == 4) {
+          o0 = make_uint2(pack_bf16x2(y[p][0], y[p][1]), pack_bf16x2(y[p][2], y[p][3]));
+          o1 = make_uint2(pack_bf16x2(y[p][4], y[p][5]), pack_bf16x2(y[p][6], y[p][7]));
+        } else {
+          o0 = pack_bf16x2(y[p][0], y[p][1]);
+          o1 = pack_bf16x2(y[p][2], y[p][3]);
+        }
       }
       uint16_t* dst = (kd[p] == 0 ? qb : (kd[p] == 1 ? kb : vb)) + gh[p] * HD;
       *reinterpret_cast<Vec*>(dst) = o0;
