@@ -19,7 +19,7 @@ namespace bca {
 namespace {
 
 constexpr int kChMin = 8;   // decode: never split a prefix into chunks shorter than 1024 keys
-constexpr int kWaves = 2;   // decode: aim for about two chunks per CTA
+constexpr int kWaves = 1;   // decode: aim for about one chunk per CTA (fewest split partials)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
