@@ -16,6 +16,13 @@
  *   an arena of promoted rows) and "Advancement 13" (canvas c attends the
  *   contiguous prefix of positions below the end of canvas c).
  *
+ * Next to the attention: "Introspective Diffusion Language Model", "3.3
+ * I-DLM Serving Stack" (short causal extends over the paged cache:
+ * bca_extend, the same rule with one-token blocks), and "Inference: Fewer,
+ * smaller forwards", "Advancement 16" (fused QKV-post before attention:
+ * bca_qkv_post; softmax-plus-argmax confidence after the LM head:
+ * bca_confidence, with "Advancement 2").
+ *
  * Every position p gets a block index blk(p) = -1 if p < P0, else
  * floor((p - P0) / D); a query at position i sees the key at position j iff
  * blk(j) <= blk(i).  Scores are scale * q.k (scale defaults to 1/sqrt(d)),
@@ -24,7 +31,8 @@
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller; bf16
- *    tensors are passed as void*.  Every pointer must be 16-byte aligned.
+ *    tensors are passed as void*.  Every pointer must be 16-byte aligned
+ *    (bca_confidence needs only element alignment, as its section says).
  *  - Layouts (row-major, innermost last):
  *      decode Q / out          [B, D, Hq, d]       k_blk, v_blk [B, D, Hkv, d]
  *      K and V pools           [num_pages, Hkv, page_size, d] (separate tensors)
