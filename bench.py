@@ -145,28 +145,50 @@ def oracle_on_sequences(seed, prefix_len, D, Hq, Hkv, d, seqs, nthreads):
     return secs, flops
 
 
-def cpu_baseline(seed, prefix_len, D, Hq, Hkv, d, budget_s=10.0):
-    import numpy as np
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(seed, prefix_len, D, Hq, Hkv, d):
+    """The fp64 oracle on the whole step: every sequence of the batch, all
+    host cores, timed once."""
     nthreads = os.cpu_count() or 1
-    order = np.random.default_rng(seed + 1000).permutation(len(prefix_len)).tolist()
-    secs = flops = 0.0
-    used = []
-    for b in order:
-        s, f = oracle_on_sequences(seed, prefix_len, D, Hq, Hkv, d, [b], nthreads)
-        secs += s
-        flops += f
-        used.append(b)
-        if secs >= budget_s:
-            break
-    keys = sum(prefix_len[b] + D for b in used)
+    secs, flops = oracle_on_sequences(seed, prefix_len, D, Hq, Hkv, d, range(len(prefix_len)),
+                                      nthreads)
+    keys = sum(prefix_len) + D * len(prefix_len)
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{len(used)} of {len(prefix_len)} sequences of the same step "
-                      f"({keys} of {sum(prefix_len) + D * len(prefix_len)} keys), fp64, "
+            "cpu_model": cpu_model(), "us_per_step": secs * 1e6,
+            "sample": f"{len(prefix_len)} of {len(prefix_len)} sequences: the whole step "
+                      f"({keys} keys), fp64 oracle with an explicit dense mask, "
                       f"{secs:.1f} s of oracle time"}
 
 
 def run_reference(args):
-    """--impl reference: the fp64 oracle, as it stands, on host cores."""
+    """--impl reference: the fp64 oracle, as it stands, on host cores.
+
+    A whole decode step takes the oracle seconds, so each timed step runs a
+    bounded sample of the step's sequences (rotating through the batch, so
+    that the run covers every sequence when it is long enough), sized to keep
+    the whole --steps/--warmup run within a few minutes.  ``value`` is the
+    oracle's measured rate; ``ms_per_step`` is the time a whole step (all 64
+    sequences) takes at that rate, and ``sample_ms_per_step`` the time of the
+    sample each step actually ran."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
@@ -174,31 +196,47 @@ def run_reference(args):
     D, Hq, Hkv, d = args.D, 32, 8, 128
     prefix_len = workloads.prefix_loguniform_blocks(64, 128, 32768, 64, args.seed)
     nthreads = os.cpu_count() or 1
-    # each step: the oracle on one sequence of the workload, the one whose
-    # estimated cost is closest to the per-step budget that keeps the whole
-    # --steps/--warmup run within a few minutes
-    budget = 150.0 / max(1, args.steps + args.warmup)
-    est_rate = 1.5e10  # fp64 flop/s of the oracle on a many-core host (estimate)
-    b_pick = min(range(64), key=lambda x: abs(4.0 * d * D * Hq * (prefix_len[x] + D) / est_rate
-                                              - budget))
-    step_seqs = [b_pick] * (args.steps + args.warmup)
+    n_steps = args.steps + args.warmup
+    budget = 150.0 / max(1, n_steps)      # seconds of oracle work per step
+    est_rate = 1.5e10                     # fp64 flop/s on a many-core host (estimate)
+    cost = [4.0 * d * D * Hq * (P + D) / est_rate for P in prefix_len]
+    order = sorted(range(64), key=lambda b: cost[b])
+    step_seqs, nxt = [], 0
+    for _ in range(n_steps):
+        picked, t = [], 0.0
+        for _ in range(64):
+            b = order[nxt % 64]
+            if picked and t + cost[b] > budget:
+                break
+            picked.append(b)
+            t += cost[b]
+            nxt += 1
+            if t >= budget:
+                break
+        step_seqs.append(picked)
     secs = flops = 0.0
-    for i, b in enumerate(step_seqs):
-        s, f = oracle_on_sequences(args.seed, prefix_len, D, Hq, Hkv, d, [b], nthreads)
+    covered = set()
+    for i, seqs in enumerate(step_seqs):
+        s, f = oracle_on_sequences(args.seed, prefix_len, D, Hq, Hkv, d, seqs, nthreads)
         if i >= args.warmup:
             secs += s
             flops += f
+            covered.update(seqs)
     value = flops / secs / 1e12 if secs > 0 else 0.0
+    step_flops = 4.0 * d * D * Hq * (sum(prefix_len) + 64 * D)
+    whole_ms = step_flops / (value * 1e12) * 1e3 if value > 0 else None
+    sample = (f"each step: {min(len(x) for x in step_seqs)}-{max(len(x) for x in step_seqs)} of "
+              f"the 64 sequences (rotating; {len(covered)} distinct sequences timed), fp64 "
+              f"oracle with an explicit dense mask; ms_per_step is a whole step at the measured "
+              f"rate")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+            "ms_per_step": whole_ms, "sample_ms_per_step": 1e3 * secs / max(1, args.steps),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(args, prefix_len),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads,
-                             "kind": "oracle",
-                             "sample": f"sequence {b_pick} of the batch (prefix "
-                                       f"{prefix_len[b_pick]}) per step, fp64 oracle with an "
-                                       "explicit dense mask"},
+                             "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -280,14 +318,41 @@ def time_steps(torch, fn, steps, stream):
     return start.elapsed_time(end)
 
 
+def prefill_row(args, bca, workloads, torch, dev, roof, time_calls, reps, res):
+    c = workloads.prefill_4x8192(seed=args.seed)
+    d = bca.dims(len(c.seq_lens), c.D, c.Hq, c.Hkv, c.d, c.pool.page_size, c.pool.num_pages,
+                 c.pool.max_pages_per_seq)
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    cu, pt = c.cu_seqlens.to(dev), c.pool.page_table.to(dev)
+    kp, vp = c.pool.k_pool.to(dev), c.pool.v_pool.to(dev)
+    out = torch.empty_like(q)
+    ws = bca.new_workspace(d, bca.OP_PREFILL, device=dev)
+    T, L = sum(c.seq_lens), max(c.seq_lens)
+    ms = time_calls(lambda: bca.bca_prefill(d, q, k, v, cu, T, L, kp, vp, pt, out, ws), reps(10))
+    pairs = sum(c.D * c.D * (L // c.D) * (L // c.D + 1) // 2 for L in c.seq_lens)
+    flops = 4.0 * c.d * c.Hq * pairs
+    bytes_ = T * (2 * c.Hq + 2 * c.Hkv) * c.d * 2.0 + 2 * T * c.Hkv * c.d * 2.0
+    res["prefill"] = dict(roof(flops, bytes_, ms), workload="4 x 8192 tokens, D=64, 32/8 heads, "
+                          "d=128, K/V written to pages of 16")
+    del q, k, v, out, kp, vp, ws
+
+
 def other_rows(args, bca, workloads, torch, pk, dev, stream):
     """The block-causal prefill (4 x 8192), the QKV-post of a decode step's
     blocks, the short causal extend (batch 64, 9 tokens) and the multicanvas step (batch 16, prompt 1024, 3 canvases of
     256; and 5 canvases under a 1024-token sliding window), each timed over repeated calls with CUDA events and set against
     its roofline: algorithmic flops (every visible (query, key) pair costs 4d
     per query head) and bytes (every input byte once, the output, page
-    writes)."""
+    writes).  Each figure is the median over calls that each start with L2
+    flushed."""
     res = {}
+    only = set(args.only.split(",")) if args.only else None
+
+    def want(name):
+        return only is None or name in only
+
+    def reps(n):
+        return args.row_reps if args.row_reps else n
 
     def roof(flops, bytes_, ms):
         t_mem = bytes_ / (pk["hbm_gbs"] * 1e9)
@@ -298,28 +363,28 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
                 "frac": max(t_mem, t_flop) / (ms * 1e-3),
                 "algorithmic_flops": flops, "algorithmic_bytes": bytes_}
 
+    # every timed call starts with a cold L2: a buffer of twice the L2 size is
+    # rewritten before it (outside the events)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
     def time_calls(fn, n):
         for _ in range(3):
             fn()
-        return time_steps(torch, fn, n, stream) / n
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
 
     # prefill: 4 sequences of 8192 tokens, D = 64, 32/8 heads, d = 128, pages written
-    c = workloads.prefill_4x8192(seed=args.seed)
-    d = bca.dims(len(c.seq_lens), c.D, c.Hq, c.Hkv, c.d, c.pool.page_size, c.pool.num_pages,
-                 c.pool.max_pages_per_seq)
-    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
-    cu, pt = c.cu_seqlens.to(dev), c.pool.page_table.to(dev)
-    kp, vp = c.pool.k_pool.to(dev), c.pool.v_pool.to(dev)
-    out = torch.empty_like(q)
-    ws = bca.new_workspace(d, bca.OP_PREFILL, device=dev)
-    T, L = sum(c.seq_lens), max(c.seq_lens)
-    ms = time_calls(lambda: bca.bca_prefill(d, q, k, v, cu, T, L, kp, vp, pt, out, ws), 10)
-    pairs = sum(c.D * c.D * (L // c.D) * (L // c.D + 1) // 2 for L in c.seq_lens)
-    flops = 4.0 * c.d * c.Hq * pairs
-    bytes_ = T * (2 * c.Hq + 2 * c.Hkv) * c.d * 2.0 + 2 * T * c.Hkv * c.d * 2.0
-    res["prefill"] = dict(roof(flops, bytes_, ms), workload="4 x 8192 tokens, D=64, 32/8 heads, "
-                          "d=128, K/V written to pages of 16")
-    del q, k, v, out, kp, vp, ws
+    if want("prefill"):
+        prefill_row(args, bca, workloads, torch, dev, roof, time_calls, reps, res)
+
 
     def mc(case, window, name, desc):
         dd = bca.dims(case.B, case.canvas_len, case.Hq, case.Hkv, case.d, case.pool.page_size,
@@ -335,7 +400,7 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         fn = lambda: bca.bca_multicanvas(dd, t["q"], t["k"], t["v"], t["lp"], t["lc"], max_live,
                                          case.prompt_len, case.n_canvas, t["kp"], t["vp"], t["pt"],
                                          t["kvp"], t["al"], None, None, 0, o, w, window=window)
-        ms2 = time_calls(fn, 20)
+        ms2 = time_calls(fn, reps(20))
         P0, C = case.prompt_len, case.canvas_len
         pairs2 = 0
         for b in range(case.B):
@@ -350,65 +415,70 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         bytes2 = (A + nl) * case.Hkv * case.d * 2 * 2.0 + 2 * nl * case.Hq * case.d * 2.0
         res[name] = dict(roof(flops2, bytes2, ms2), workload=desc)
 
-    # QKV-post: batch 64 blocks of 64 tokens after the serving prefixes,
-    # 32/8 heads, d = 128, norms + RoPE, the key / value rows written to pages
-    Pq = workloads.prefix_loguniform_blocks(64, 128, 32768, 64, seed=args.seed)
-    cq = workloads.make_qkv_post_case(64, 64, 32, 8, 128, prefix_len=Pq, seed=args.seed)
-    dq = bca.dims(cq.B, cq.n, cq.Hq, cq.Hkv, cq.d, cq.pool.page_size, cq.pool.num_pages,
-                  cq.pool.max_pages_per_seq)
-    tq = {k_: v_.to(dev) for k_, v_ in (("qkv", cq.qkv), ("pos", cq.positions),
-                                        ("qw", cq.q_norm_w), ("kw", cq.k_norm_w),
-                                        ("wp", cq.write_pos), ("kp", cq.pool.k_pool),
-                                        ("vp", cq.pool.v_pool), ("pt", cq.pool.page_table))}
-    oq = torch.empty((cq.B, cq.n, cq.Hq, cq.d), dtype=torch.bfloat16, device=dev)
-    ok_ = torch.empty((cq.B, cq.n, cq.Hkv, cq.d), dtype=torch.bfloat16, device=dev)
-    ov = torch.empty_like(ok_)
-    wq = bca.new_workspace(dq, bca.OP_COMMIT, device=dev)
-    ms_q = time_calls(lambda: bca.bca_qkv_post(dq, tq["qkv"], tq["pos"], oq, ok_, ov, wq,
-                                               q_norm_w=tq["qw"], k_norm_w=tq["kw"], eps=1e-6,
-                                               rope_theta=1e6, write_pos=tq["wp"],
-                                               k_pool=tq["kp"], v_pool=tq["vp"],
-                                               page_table=tq["pt"]), 50)
-    tokens = cq.B * cq.n
-    row = (cq.Hq + 2 * cq.Hkv) * cq.d * 2.0
-    bytes_q = tokens * (2 * row + 2 * cq.Hkv * cq.d * 2.0 + 8.0) + 2 * cq.d * 2.0
-    res["qkv_post"] = dict(roof(0.0, bytes_q, ms_q),
-                           workload="batch 64 x 64 tokens after the serving prefixes, 32/8 heads, "
-                                    "d=128: per-head RMS norms + RoPE (theta 1e6) of q and k, "
-                                    "K/V rows written to pages of 16")
-    del tq, oq, ok_, ov, wq, cq
+    if want("qkv_post"):
+        # QKV-post: batch 64 blocks of 64 tokens after the serving prefixes,
+        # 32/8 heads, d = 128, norms + RoPE, the key / value rows written to pages
+        Pq = workloads.prefix_loguniform_blocks(args.row_batch, 128, 32768, 64, seed=args.seed)
+        cq = workloads.make_qkv_post_case(args.row_batch, 64, 32, 8, 128, prefix_len=Pq,
+                                              seed=args.seed)
+        dq = bca.dims(cq.B, cq.n, cq.Hq, cq.Hkv, cq.d, cq.pool.page_size, cq.pool.num_pages,
+                      cq.pool.max_pages_per_seq)
+        tq = {k_: v_.to(dev) for k_, v_ in (("qkv", cq.qkv), ("pos", cq.positions),
+                                            ("qw", cq.q_norm_w), ("kw", cq.k_norm_w),
+                                            ("wp", cq.write_pos), ("kp", cq.pool.k_pool),
+                                            ("vp", cq.pool.v_pool), ("pt", cq.pool.page_table))}
+        oq = torch.empty((cq.B, cq.n, cq.Hq, cq.d), dtype=torch.bfloat16, device=dev)
+        ok_ = torch.empty((cq.B, cq.n, cq.Hkv, cq.d), dtype=torch.bfloat16, device=dev)
+        ov = torch.empty_like(ok_)
+        wq = bca.new_workspace(dq, bca.OP_COMMIT, device=dev)
+        ms_q = time_calls(lambda: bca.bca_qkv_post(dq, tq["qkv"], tq["pos"], oq, ok_, ov, wq,
+                                                   q_norm_w=tq["qw"], k_norm_w=tq["kw"], eps=1e-6,
+                                                   rope_theta=1e6, write_pos=tq["wp"],
+                                                   k_pool=tq["kp"], v_pool=tq["vp"],
+                                                   page_table=tq["pt"]), reps(50))
+        tokens = cq.B * cq.n
+        row = (cq.Hq + 2 * cq.Hkv) * cq.d * 2.0
+        bytes_q = tokens * (2 * row + 2 * cq.Hkv * cq.d * 2.0 + 8.0) + 2 * cq.d * 2.0
+        res["qkv_post"] = dict(roof(0.0, bytes_q, ms_q),
+                               workload=f"batch {cq.B} x 64 tokens after the serving prefixes, 32/8 heads, "
+                                        "d=128: per-head RMS norms + RoPE (theta 1e6) of q and k, "
+                                        "K/V rows written to pages of 16")
+        del tq, oq, ok_, ov, wq, cq
 
-    # short causal extend: batch 64, 9 new tokens (2N-1, N = 5), prefixes at
-    # token granularity, 32/8 heads, d = 128, the new rows committed
-    P = workloads.prefix_loguniform_blocks(64, 128, 32768, 1, seed=args.seed)
-    n = 9
-    ce = workloads.make_decode_case(P, D=n, Hq=32, Hkv=8, d=128, seed=args.seed,
-                                    keep_logical=False)
-    de = bca.dims(ce.B, n, ce.Hq, ce.Hkv, ce.d, ce.pool.page_size, ce.pool.num_pages,
-                  ce.pool.max_pages_per_seq)
-    te = {"q": ce.q.to(dev), "k": ce.k_blk.to(dev), "v": ce.v_blk.to(dev),
-          "kp": ce.pool.k_pool.to(dev), "vp": ce.pool.v_pool.to(dev),
-          "pt": ce.pool.page_table.to(dev),
-          "pl": torch.tensor(P, dtype=torch.int32, device=dev)}
-    oe = torch.empty_like(te["q"])
-    we = bca.new_workspace(de, bca.OP_DECODE, device=dev)
-    ms_e = time_calls(lambda: bca.bca_extend(de, te["q"], te["k"], te["v"], te["kp"], te["vp"],
-                                             te["pt"], te["pl"], oe, True, we), 20)
-    pairs_e = sum(p_ * n + n * (n + 1) // 2 for p_ in P)
-    flops_e = 4.0 * ce.d * ce.Hq * pairs_e
-    kv_row = 2 * ce.Hkv * ce.d * 2.0  # K and V bytes of one token
-    bytes_e = (sum(P) * kv_row + ce.B * n * (2 * ce.Hq * ce.d * 2.0 + 2 * kv_row)
-               + ce.B * ce.pool.max_pages_per_seq * 4.0)
-    res["extend"] = dict(roof(flops_e, bytes_e, ms_e),
-                         workload=f"batch 64, 9 new causal tokens after log-uniform prefixes in "
-                                  f"[128, 32768] (sum {sum(P)}), 32/8 heads, d=128, page 16, "
-                                  f"new rows committed")
-    del te, oe, we, ce
+    if want("extend"):
+        # short causal extend: batch 64, 9 new tokens (2N-1, N = 5), prefixes at
+        # token granularity, 32/8 heads, d = 128, the new rows committed
+        P = workloads.prefix_loguniform_blocks(args.row_batch, 128, 32768, 1, seed=args.seed)
+        n = 9
+        ce = workloads.make_decode_case(P, D=n, Hq=32, Hkv=8, d=128, seed=args.seed,
+                                        keep_logical=False)
+        de = bca.dims(ce.B, n, ce.Hq, ce.Hkv, ce.d, ce.pool.page_size, ce.pool.num_pages,
+                      ce.pool.max_pages_per_seq)
+        te = {"q": ce.q.to(dev), "k": ce.k_blk.to(dev), "v": ce.v_blk.to(dev),
+              "kp": ce.pool.k_pool.to(dev), "vp": ce.pool.v_pool.to(dev),
+              "pt": ce.pool.page_table.to(dev),
+              "pl": torch.tensor(P, dtype=torch.int32, device=dev)}
+        oe = torch.empty_like(te["q"])
+        we = bca.new_workspace(de, bca.OP_DECODE, device=dev)
+        ms_e = time_calls(lambda: bca.bca_extend(de, te["q"], te["k"], te["v"], te["kp"], te["vp"],
+                                                 te["pt"], te["pl"], oe, True, we), reps(20))
+        pairs_e = sum(p_ * n + n * (n + 1) // 2 for p_ in P)
+        flops_e = 4.0 * ce.d * ce.Hq * pairs_e
+        kv_row = 2 * ce.Hkv * ce.d * 2.0  # K and V bytes of one token
+        bytes_e = (sum(P) * kv_row + ce.B * n * (2 * ce.Hq * ce.d * 2.0 + 2 * kv_row)
+                   + ce.B * ce.pool.max_pages_per_seq * 4.0)
+        res["extend"] = dict(roof(flops_e, bytes_e, ms_e),
+                             workload=f"batch {ce.B}, 9 new causal tokens after log-uniform prefixes in "
+                                      f"[128, 32768] (sum {sum(P)}), 32/8 heads, d=128, page 16, "
+                                      f"new rows committed")
+        del te, oe, we, ce
 
-    mc(workloads.multicanvas_b16(seed=args.seed), 0, "multicanvas",
-       "batch 16, prompt 1024, 3 canvases of 256 with 30-100% live rows, 32/8 heads, d=128")
-    mc(workloads.make_multicanvas_case(16, 1024, 5, 256, 32, 8, 128, seed=args.seed), 1024,
-       "multicanvas_window", "as above with 5 canvases under a 1024-token sliding window")
+    if want("multicanvas"):
+        mc(workloads.multicanvas_b16(seed=args.seed), 0, "multicanvas",
+           "batch 16, prompt 1024, 3 canvases of 256 with 30-100% live rows, 32/8 heads, d=128")
+    if want("multicanvas_window"):
+        mc(workloads.make_multicanvas_case(16, 1024, 5, 256, 32, 8, 128, seed=args.seed), 1024,
+           "multicanvas_window", "as above with 5 canvases under a 1024-token sliding window")
     return res
 
 
@@ -433,9 +503,17 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def build_case(D):
+    if args.only:
+        rows = other_rows(args, bca, workloads, torch, pk, dev, stream)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "other_rows": rows}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    def build_case(D, seed):
         # each rank runs its own batch (weak scaling): seed offset by rank
-        case = workloads.serving_decode(seed=rank_seed(args.seed, rank), D=D, B=args.batch,
+        case = workloads.serving_decode(seed=rank_seed(seed, rank), D=D, B=args.batch,
                                         keep_logical=False)
         S = case.pool.page_size
         dd = bca.dims(case.B, D, case.Hq, case.Hkv, case.d, S, case.pool.num_pages,
@@ -452,8 +530,8 @@ def run_ours(args):
         return lambda: bca.bca_decode(dd, t["q"], t["kb"], t["vb"], t["kp"], t["vp"], t["pt"],
                                       t["pl"], t["out"], True, t["ws"])
 
-    def measure(D, steps, warmup, with_clocks):
-        case, dd, t = build_case(D)
+    def measure(D, steps, warmup, with_clocks, seed=args.seed):
+        case, dd, t = build_case(D, seed)
         step = step_fn(dd, t)
         for _ in range(warmup):
             step()
@@ -563,6 +641,24 @@ def run_ours(args):
         del lg
     rows_line = other_rows(args, bca, workloads, torch, pk, dev, stream) if not args.no_sweep else None
 
+    # the headline step on two more seeded batches (prefix lengths differ)
+    seeds = [{"seed": args.seed, "us_per_step": ms_max * 1e3, "attn_us": attn_avg_ms * 1e3,
+              "attn_hbm_frac": roofline["frac"],
+              "step_roofline_frac": roofline["step_roofline_frac"], "sum_prefix": alg["sum_prefix"]}]
+    if not args.no_sweep:
+        for sd in (args.seed + 1, args.seed + 2):
+            c3, _, t3, ms3, _, prof3, alg3 = measure(args.D, max(20, args.steps // 4),
+                                                     max(3, args.warmup), False, seed=sd)
+            n3, tot3 = prof3["attention"]
+            a3 = tot3 / max(1, n3)
+            seeds.append({"seed": sd, "us_per_step": ms3 * 1e3, "attn_us": a3 * 1e3,
+                          "attn_hbm_frac": alg3["attn_bytes"] / (a3 * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "step_roofline_frac": max(alg3["step_bytes"] / (pk["hbm_gbs"] * 1e9),
+                                                    alg3["flops"] / (pk["bf16_tflops"] * 1e12))
+                                                / (ms3 * 1e-3),
+                          "sum_prefix": alg3["sum_prefix"]})
+            del t3, c3
+
     sweep = []
     if not args.no_sweep:
         for D2 in (32, 64):
@@ -583,7 +679,7 @@ def run_ours(args):
     if rank == 0:
         prefix_len = workloads.prefix_loguniform_blocks(args.batch, 128, 32768, 64, args.seed)
         cpu = None if args.no_cpu_baseline else cpu_baseline(args.seed, prefix_len, args.D, 32, 8,
-                                                             128, args.cpu_seconds)
+                                                             128)
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
                 "us_per_step": ms_max * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -596,7 +692,8 @@ def run_ours(args):
                 "gpu_launches": int(round(launches_per_step * args.steps)),
                 "launches_per_step": launches_per_step,
                 "kernel_ms": {k: (v[1] / v[0] if v[0] else None) for k, v in prof.items()},
-                "clocks": clocks, "device_status": st, "sweep": sweep, "confidence": conf_line,
+                "clocks": clocks, "device_status": st, "seeds": seeds, "sweep": sweep,
+                "confidence": conf_line,
                 "other_rows": rows_line}
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -618,7 +715,13 @@ def main():
                          "batches are for profiler captures)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", default=None,
+                    help="run only these secondary rows (comma list of prefill, qkv_post, extend, "
+                         "multicanvas, multicanvas_window) and print them; for profiler captures")
+    ap.add_argument("--row-reps", type=int, default=0,
+                    help="timed calls per secondary row (0: the row's default)")
+    ap.add_argument("--row-batch", type=int, default=64,
+                    help="sequences of the QKV-post and extend rows (64 is the benchmarked size)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture (reported as is)")
     args = ap.parse_args()

@@ -35,6 +35,7 @@
 //               (bf16) back into the S columns, final normalisation and store.
 // Every wait is bounded; on timeout the CTA records BCA_ERR_DEVICE_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
+#include <atomic>
 #include <climits>
 #include <cstdint>
 
@@ -1309,10 +1310,17 @@ template <int HD, bool kBand>
 cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int grid,
                                 cudaStream_t stream) {
   using C = Cfg<HD>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD, kBand>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+  // The shared-memory attribute is a property of the kernel on one device:
+  // set it once per device (several host threads may get here at once; a
+  // repeated set is harmless).
+  static std::atomic<bool> configured[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (!cached || !configured[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(attention_kernel<HD, kBand>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     // setmaxnreg.inc waits for registers released by setmaxnreg.dec; the
     // split must fit what the block is launched with, or the kernel would stall
@@ -1320,7 +1328,7 @@ cudaError_t launch_attention_hd(const AttnParams& p, const AttnMaps& maps, int g
     e = cudaFuncGetAttributes(&fa, attention_kernel<HD, kBand>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
-    configured = true;
+    if (cached) configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

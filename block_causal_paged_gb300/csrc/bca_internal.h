@@ -14,6 +14,7 @@ constexpr int kChunksPerTile = kTileKeys / kChunkKeys;
 constexpr int kRowsPerMTile = 128;
 constexpr int kThreads = 384;     // 12 warps, see the role map in attention.cu
 constexpr int kFusedPlanMax = 64; // decode batches up to this are planned inside the attention kernel
+constexpr int kMaxDevices = 64;   // per-device launch caches (device ordinals beyond: no cache)
 // Per internal wait: about 2 s at the maximum SM clock (longer when clocked down).
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
 

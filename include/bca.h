@@ -277,10 +277,10 @@ int bca_commit_kv(const bca_dims* dims, const void* k_blk, const void* v_blk, vo
  *
  * "Inference for Interpretable Text-Diffusion Models", "KV Cache", step 1 and
  * the prefill BlockMask figure: P0 = 0, every token attends its own block
- * bidirectionally and earlier blocks causally.  Key tiles of 64 are
- * classified per query tile of 128 as fully included (no mask), partially
- * included (elementwise mask) or fully excluded (never loaded)
- * ("FlexAttention with Aligned Tiles").
+ * bidirectionally and earlier blocks causally.  Tiles of 128 queries x 128
+ * keys are classified as fully included (no mask), partially included
+ * (elementwise mask) or fully excluded (never loaded) ("FlexAttention with
+ * Aligned Tiles"); with D = 64 each diagonal tile is partial (3/4 visible).
  *
  * Packed layout: q/out [total_tokens, Hq, d], k/v [total_tokens, Hkv, d];
  * sequence b occupies rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (int32 [B+1],

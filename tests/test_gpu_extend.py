@@ -54,17 +54,15 @@ def test_one_token_extend_equals_one_token_decode(cuda_lib):
 
 def test_serving_extend_b64_n9(cuda_lib):
     """Batch 64, 9 new tokens (N = 5), prefixes log-uniform in [128, 32768]
-    at token granularity: the bench workload; sampled sequences against the
-    oracle (the longest, the shortest and one in between), every row."""
+    at token granularity: the bench workload; every sequence against the
+    oracle, every row."""
     P = workloads.prefix_loguniform_blocks(64, 128, 32768, 1, seed=0)
     case = workloads.make_decode_case(P, D=9, Hq=32, Hkv=8, d=128, seed=0)
     r = DecodeRun(case)
     out = r.run(extend=True)
     assert r.status() == 0
-    order = np.argsort(P)
-    seqs = [int(order[-1]), int(order[0]), int(order[len(P) // 2])]
-    ref = _ref(case, seqs=seqs)
-    for b in seqs:
+    ref = _ref(case)
+    for b in range(len(P)):
         assert_close(out[b], ref[b], what=f"serving extend seq {b} P={P[b]}")
 
 

@@ -61,6 +61,54 @@ def test_prefill_4x8192_sampled_rows_and_tile_counts(cuda_lib):
     assert skipped == per * int((cls == "S").sum())
 
 
+def test_prefill_full_sequence_every_row(cuda_lib):
+    """One whole 8192-token sequence of the 4 x 8192 workload (seed 1), every
+    query row of every head against the oracle."""
+    case = workloads.prefill_4x8192(seed=1)
+    r = PrefillRun(case, write_pages=False)
+    out = r.run()
+    assert r.status() == 0
+    b = 2
+    ref = _ref(case, q_rows={b: np.arange(8192)})
+    cu = case.cu_seqlens.tolist()
+    assert_close(out[cu[b]:cu[b + 1]], ref[cu[b]:cu[b + 1]], what=f"seq {b}, all rows")
+
+
+def test_appending_a_block_leaves_completed_blocks_unchanged(cuda_lib):
+    """A completed block's outputs cannot change when later blocks are added
+    ("Inference for Interpretable Text-Diffusion Models", "Background"): the
+    prefill of T tokens and of the same tokens plus one more block of D give
+    bit-identical rows for the first T tokens (the same tiles are computed
+    for them; the added keys are never visible to them)."""
+    D, T = 64, 1024
+    big = workloads.make_prefill_case([T + D], D=D, Hq=16, Hkv=4, d=128, seed=41)
+    small = workloads.make_prefill_case([T], D=D, Hq=16, Hkv=4, d=128, seed=41)
+    small.q.copy_(big.q[:T])
+    small.k.copy_(big.k[:T])
+    small.v.copy_(big.v[:T])
+    a = PrefillRun(small, write_pages=False).run().cpu()
+    bb = PrefillRun(big, write_pages=False).run().cpu()
+    assert torch.equal(a.view(torch.int16), bb[:T].view(torch.int16))
+    assert_close(a, _ref(small), what="prefill of T tokens")
+
+
+def test_prefill_within_block_permutation_equivariance(cuda_lib):
+    """Permuting the tokens inside each block of a prompt (queries, keys and
+    values together) permutes the prefill outputs the same way."""
+    D, T = 64, 640
+    case = workloads.make_prefill_case([T], D=D, Hq=8, Hkv=2, d=128, seed=43)
+    base = PrefillRun(case, write_pages=False).run().cpu().clone()
+    g = torch.Generator().manual_seed(43)
+    perm = torch.cat([j * D + torch.randperm(D, generator=g) for j in range(T // D)])
+    pc = workloads.make_prefill_case([T], D=D, Hq=8, Hkv=2, d=128, seed=43)
+    pc.q.copy_(case.q[perm])
+    pc.k.copy_(case.k[perm])
+    pc.v.copy_(case.v[perm])
+    got = PrefillRun(pc, write_pages=False).run().cpu()
+    assert_close(got, base[perm].double().numpy(), what="permuted vs unpermuted")
+    assert_close(got, _ref(pc), what="permuted vs oracle")
+
+
 def test_decode_block_equals_prefill_rows(cuda_lib):
     """decode(block j | prefix) on the GPU equals the GPU prefill rows of block j
     within the tolerance (both against the same oracle values)."""

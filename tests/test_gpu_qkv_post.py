@@ -133,3 +133,22 @@ def test_serving_block_b64(cuda_lib):
     r.run()
     assert r.status() == 0
     _check(r)
+
+
+@pytest.mark.parametrize("scale,eps", [(1e-3, 1e-6), (3e-4, 1e-5)])
+def test_small_rows_where_epsilon_matters(cuda_lib, scale, eps):
+    """Rows small enough that the norm's epsilon is as large as (or larger
+    than) the mean of the squares: the kernel follows the oracle's
+    x * w / sqrt(mean(x^2) + eps), and the same comparison with eps dropped
+    from the oracle fails, so the term is really exercised."""
+    c = workloads.make_qkv_post_case(4, 16, 8, 2, 128, prefix_len=[0, 64, 320, 4032], seed=9,
+                                     qkv_scale=scale)
+    r = Run(c)
+    r.run(eps=eps)
+    assert r.status() == 0
+    _check(r, eps=eps)
+    q0, _, _ = oracle.qkv_post(c.qkv, c.positions, c.Hq, c.Hkv, q_norm_w=c.q_norm_w,
+                               k_norm_w=c.k_norm_w, eps=0.0, rope_theta=1e6)
+    g = r.q.float().cpu().numpy().astype(np.float64)
+    bound = 2.0 ** -8 * np.abs(q0) + 2.0 ** -16
+    assert (np.abs(g - q0) > bound).mean() > 0.5

@@ -90,3 +90,49 @@ def test_norm_before_rotation():
     nq = (x[:, :1] * w / torch.sqrt((x[:, :1] ** 2).mean(-1, keepdim=True))).numpy()
     r, _, _ = oracle.qkv_post(torch.from_numpy(nq), pos, 1, 0, rope_theta=100.0)
     assert np.abs(q - r).max() < 1e-12
+
+
+def test_rms_norm_epsilon_closed_forms():
+    """The epsilon of the RMS norm sits inside the square root, added to the
+    mean of the squares (not scaled by d, not outside the root).  A constant
+    head vector x = c with weight 1 normalises to c / sqrt(c^2 + eps); with
+    c = 1e-3 and eps = 1e-6 the two terms are equal, so any other placement
+    of eps moves the result far from 1/sqrt(2)."""
+    d = 64
+    c, eps = 1e-3, 1e-6
+    x = torch.full((3, 2, d), c, dtype=torch.float64)
+    w = torch.ones(d, dtype=torch.float64)
+    q, k, _ = oracle.qkv_post(x, torch.zeros(3, dtype=torch.long), 1, 0, q_norm_w=w, eps=eps)
+    want = c / math.sqrt(c * c + eps)
+    assert abs(want - 1.0 / math.sqrt(2.0)) < 1e-12
+    assert np.abs(q - want).max() < 1e-12
+    # the slips a reader could make all give other numbers
+    assert abs(c / (math.sqrt(c * c) + eps) - want) > 1e-3          # eps outside the root
+    assert abs(c / math.sqrt(c * c + d * eps) - want) > 1e-2        # eps scaled by d
+    assert abs(c / math.sqrt(c * c + eps / d) - want) > 1e-2        # eps divided by d
+    # eps dominating: x tiny against sqrt(eps) gives x / sqrt(eps) to first order
+    x2 = torch.full((1, 1, d), 1e-9, dtype=torch.float64)
+    q2, _, _ = oracle.qkv_post(x2, torch.zeros(1, dtype=torch.long), 1, 0, q_norm_w=w, eps=1e-2)
+    assert np.abs(q2 - 1e-9 / math.sqrt(1e-18 + 1e-2)).max() < 1e-20
+    # the key heads use their own weight, with the same epsilon
+    xk = torch.cat([x, x], dim=1)
+    _, k2, _ = oracle.qkv_post(xk, torch.zeros(3, dtype=torch.long), 1, 1, k_norm_w=2.0 * w,
+                               eps=eps)
+    assert np.abs(k2 - 2.0 * want).max() < 1e-12
+
+
+def test_rms_norm_epsilon_non_uniform_weight_and_vector():
+    """Non-uniform x and w with eps of the same size as mean(x^2): the output
+    is w_i x_i / sqrt(mean(x^2) + eps), checked against sums written out in
+    plain Python for a 4-element head."""
+    xs = [3e-3, -1e-3, 2e-3, 0.0]
+    ws = [0.5, 1.5, -2.0, 4.0]
+    eps = 4e-6
+    ms = sum(v * v for v in xs) / 4.0          # 3.5e-6, same order as eps
+    x = torch.tensor([[xs]], dtype=torch.float64)
+    w = torch.tensor(ws, dtype=torch.float64)
+    q, _, _ = oracle.qkv_post(x, torch.zeros(1, dtype=torch.long), 1, 0, q_norm_w=w, eps=eps)
+    want = [wi * xi / math.sqrt(ms + eps) for xi, wi in zip(xs, ws)]
+    assert np.abs(q[0, 0] - np.array(want)).max() < 1e-15
+    # and eps = 0 would have given a result about 1.46x larger
+    assert abs(want[0] / (ws[0] * xs[0] / math.sqrt(ms)) - math.sqrt(ms / (ms + eps))) < 1e-12
