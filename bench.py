@@ -183,9 +183,10 @@ def run_reference(args):
     """--impl reference: the fp64 oracle, as it stands, on host cores.
 
     A whole decode step takes the oracle seconds, so each timed step runs a
-    bounded sample of the step's sequences (rotating through the batch, so
-    that the run covers every sequence when it is long enough), sized to keep
-    the whole --steps/--warmup run within a few minutes.  ``value`` is the
+    bounded sample of the step's sequences: the timed steps cover the batch
+    once, cheapest sequences first and several per step while they fit the
+    step's budget, then repeat the cheapest one, so that the whole
+    --steps/--warmup run stays within a few minutes.  ``value`` is the
     oracle's measured rate; ``ms_per_step`` is the time a whole step (all 64
     sequences) takes at that rate, and ``sample_ms_per_step`` the time of the
     sample each step actually ran."""
@@ -201,19 +202,21 @@ def run_reference(args):
     est_rate = 1.5e10                     # fp64 flop/s on a many-core host (estimate)
     cost = [4.0 * d * D * Hq * (P + D) / est_rate for P in prefix_len]
     order = sorted(range(64), key=lambda b: cost[b])
-    step_seqs, nxt = [], 0
-    for _ in range(n_steps):
+    # the warm-up steps run the cheapest sequence; the timed steps then cover
+    # the batch once (cheapest first, several sequences per step while they
+    # fit the step's budget, an expensive one alone), after which each step
+    # repeats the cheapest sequence
+    step_seqs, nxt = [[order[0]]] * args.warmup, 0
+    for _ in range(args.steps):
         picked, t = [], 0.0
-        for _ in range(64):
-            b = order[nxt % 64]
+        while nxt < 64:
+            b = order[nxt]
             if picked and t + cost[b] > budget:
                 break
             picked.append(b)
             t += cost[b]
             nxt += 1
-            if t >= budget:
-                break
-        step_seqs.append(picked)
+        step_seqs.append(picked or [order[0]])
     secs = flops = 0.0
     covered = set()
     for i, seqs in enumerate(step_seqs):
@@ -225,10 +228,10 @@ def run_reference(args):
     value = flops / secs / 1e12 if secs > 0 else 0.0
     step_flops = 4.0 * d * D * Hq * (sum(prefix_len) + 64 * D)
     whole_ms = step_flops / (value * 1e12) * 1e3 if value > 0 else None
-    sample = (f"each step: {min(len(x) for x in step_seqs)}-{max(len(x) for x in step_seqs)} of "
-              f"the 64 sequences (rotating; {len(covered)} distinct sequences timed), fp64 "
-              f"oracle with an explicit dense mask; ms_per_step is a whole step at the measured "
-              f"rate")
+    sample = (f"each timed step: {min(len(x) for x in step_seqs[args.warmup:])}-"
+              f"{max(len(x) for x in step_seqs[args.warmup:])} of the 64 sequences ("
+              f"{len(covered)} distinct sequences timed over the run), fp64 oracle with an "
+              f"explicit dense mask; ms_per_step is a whole step at the measured rate")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": whole_ms, "sample_ms_per_step": 1e3 * secs / max(1, args.steps),
