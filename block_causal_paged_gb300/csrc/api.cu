@@ -1,8 +1,10 @@
 // C ABI of the library: argument checks, workspace layout, TMA descriptor
 // encoding (with a small cache) and kernel launches.  Declarations and the
 // contract of every entry point are in include/bca.h.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -45,6 +47,29 @@ float scale_log2(const bca_dims* d) {
   const double s = d->softmax_scale > 0.0f ? (double)d->softmax_scale
                                            : 1.0 / std::sqrt((double)d->head_dim);
   return (float)(s * 1.4426950408889634);  // log2(e)
+}
+
+// The CTA-pair attention kernel is used wherever it applies, unless the
+// environment sets BCA_PAIR_KERNEL=0 (read at each call; the single-CTA
+// kernel then runs every shape, with results equal within rounding).
+bool pair_kernel_enabled() {
+  const char* v = std::getenv("BCA_PAIR_KERNEL");
+  return !(v && v[0] == '0' && v[1] == '\0');
+}
+
+// Resident pairs of the pair kernel on the current device (cached per device).
+int pair_capacity(int sms) {
+  static std::atomic<int> cap[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= kMaxDevices) return attention_pair_max_pairs(sms);
+  int n = cap[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    n = attention_pair_max_pairs(sms);
+    if (n <= 0) return 0;
+    cap[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 struct DeviceInfo {
@@ -503,14 +528,26 @@ int decode_impl(const bca_dims* d, const void* q, const void* k_blk, const void*
   const long long max_tiles = ceil_div_i(cap_tokens, kTileKeys) + ceil_div_i(d->block_size, kTileKeys);
   const long long max_items =
       (long long)d->batch * d->num_kv_heads * p.n_rb * ceil_div_i(max_tiles, kChMin);
-  const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
+  int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
+  // CTA pairs: decode blocks whose first row block fills both M-tiles, made
+  // of whole 16-key chunks (so every page box is whole), head_dim 128
+  int n_pairs = 0;
+  if (pair_kernel_enabled() && HD == 128 && !causal && d->block_size % kChunkKeys == 0 &&
+      d->block_size > p.tpm) {
+    n_pairs = (int)std::min<long long>(pair_capacity(di.sms), std::max<long long>(1, max_items));
+    p.pair = n_pairs > 0 ? 1 : 0;
+  }
+  const int units = p.pair ? n_pairs : grid;
   cudaStream_t s = (cudaStream_t)stream;
   // small batches are planned inside the attention kernel (no plan launch)
   p.fused_plan = d->batch <= kFusedPlanMax ? 1 : 0;
   if (!p.fused_plan &&
-      timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
+      timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, units, s); }) != cudaSuccess)
     return BCA_ERR_CUDA;
-  if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
+  if (timed(BCA_KERNEL_ATTENTION, s, [&] {
+        return p.pair ? launch_attention_pair(p, maps, n_pairs, s)
+                      : launch_attention(p, maps, HD, grid, s);
+      }) != cudaSuccess)
     return BCA_ERR_CUDA;
   // epilogue: the commit (if asked) and the split-KV combine (if any prefix can split)
   if (commit || max_tiles > kChMin) {
@@ -583,10 +620,20 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
   const long long max_items = (long long)d->batch * ceil_div_i(max_seqlen, 128) *
                               d->num_kv_heads * p.n_hp;
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
+  // CTA pairs: two query heads per item (G >= 2), head_dim 128
+  int n_pairs = 0;
+  if (pair_kernel_enabled() && HD == 128 && p.G >= 2) {
+    n_pairs = (int)std::min<long long>(pair_capacity(di.sms), std::max<long long>(1, max_items));
+    p.pair = n_pairs > 0 ? 1 : 0;
+  }
   cudaStream_t s = (cudaStream_t)stream;
-  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
+  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, p.pair ? n_pairs : grid, s); }) !=
+      cudaSuccess)
     return BCA_ERR_CUDA;
-  if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
+  if (timed(BCA_KERNEL_ATTENTION, s, [&] {
+        return p.pair ? launch_attention_pair(p, maps, n_pairs, s)
+                      : launch_attention(p, maps, HD, grid, s);
+      }) != cudaSuccess)
     return BCA_ERR_CUDA;
   if (k_pool) {
     CommitParams c;

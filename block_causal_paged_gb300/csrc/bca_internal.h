@@ -31,7 +31,10 @@ struct WsHeader {
   unsigned long long tiles_skipped;
   int32_t n_split_slots;   // decode: split-KV slots in use (plan)
   int32_t exit_count;      // attention CTAs finished in the current launch (reset by the last)
-  int32_t reserved1[52];
+  // the first internal wait that timed out: 1 once recorded, the CTA, the warp,
+  // the barrier's byte offset in the CTA's shared memory and the awaited parity
+  int32_t wait_fail[5];
+  int32_t reserved1[47];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 constexpr size_t kWsHeaderBytes = 256;
@@ -59,6 +62,7 @@ struct AttnParams {
   int n_rb;            // decode: row blocks per KV head (each = 2 M-tiles)
   int ch_min, waves;   // decode split policy
   int fused_plan;      // decode: every CTA plans for itself (batch <= kFusedPlanMax)
+  int pair;            // launched on CTA pairs (attention_pair.cu): one work unit per pair
   int causal;          // decode: the D query tokens attend each other causally (short
                        // extend; the prefix length then need not be a multiple of D)
   int n_qt_max;        // prefill: query tiles of the longest sequence (host bound)
@@ -111,6 +115,14 @@ cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream)
 // Launch the block-causal attention kernel (decode, prefill or multicanvas).
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head_dim, int grid,
                              cudaStream_t stream);
+
+// Launch the CTA-pair attention kernel (decode with D a multiple of 16 and at
+// least two M-tiles per item, or prefill; head_dim 128) on n_pairs clusters of
+// two CTAs.
+cudaError_t launch_attention_pair(const AttnParams& p, const AttnMaps& maps, int n_pairs,
+                                  cudaStream_t stream);
+// Clusters of two CTAs of that kernel that can be resident at once (0 on error).
+int attention_pair_max_pairs(int n_sms);
 
 // Split-KV combine for decode: one CTA per (split group, 32 head-dim columns),
 // over the slot table the plan kernel wrote.

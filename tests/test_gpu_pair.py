@@ -1,0 +1,111 @@
+"""The CTA-pair attention kernel (decode blocks of >= 2 M-tiles, prefill;
+head_dim 128) against the fp64 oracle and against the single-CTA kernel on
+the same inputs (BCA_PAIR_KERNEL=0 routes every shape to the latter)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _gpu_cases import DecodeRun, PrefillRun, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+class single_cta_kernel:
+    """Context manager: run the library with the pair kernel disabled."""
+
+    def __enter__(self):
+        self.old = os.environ.get("BCA_PAIR_KERNEL")
+        os.environ["BCA_PAIR_KERNEL"] = "0"
+
+    def __exit__(self, *exc):
+        if self.old is None:
+            os.environ.pop("BCA_PAIR_KERNEL", None)
+        else:
+            os.environ["BCA_PAIR_KERNEL"] = self.old
+
+
+def _decode_ref(case, seqs=None):
+    return oracle.decode(case.q, case.k_blk, case.v_blk, case.k_prefix, case.v_prefix, seqs=seqs)
+
+
+@pytest.mark.parametrize("P,D,Hq,Hkv", [
+    ([128, 512], 64, 32, 8),                  # the serving shape, two short prefixes
+    ([0, 64, 4096, 960], 64, 32, 8),          # empty prefix; a 64-key last prefix tile
+    ([96 * 3, 96 * 40], 96, 32, 8),           # second row block with one M-tile only
+    ([48 * 7, 48 * 100, 0], 48, 32, 8),       # second M-tile of 16 tokens
+    ([64 * 11, 64 * 300], 64, 64, 8),         # G = 8: two row blocks per KV head
+    ([32 * 5, 32 * 77], 32, 16, 8),           # G = 2, D = 32: one M-tile, single-CTA kernel
+    ([2048, 30080], 128, 32, 8),              # D = 128: two row blocks, a full own tile
+])
+def test_pair_decode_matches_oracle_and_single_cta(cuda_lib, P, D, Hq, Hkv):
+    case = workloads.make_decode_case(P, D=D, Hq=Hq, Hkv=Hkv, d=128, seed=51)
+    r = DecodeRun(case)
+    got = r.run().clone()
+    assert r.status() == 0
+    ref = _decode_ref(case)
+    assert_close(got, ref, what=f"pair decode P={P} D={D} {Hq}/{Hkv}")
+    with single_cta_kernel():
+        one = r.run().clone()
+    assert r.status() == 0
+    assert_close(one, ref, what="single-CTA decode")
+    diff = (got.double() - one.double()).abs()
+    assert float(diff.max()) <= 2e-2 and float(diff.mean()) <= 2e-3
+
+
+def test_pair_decode_serving_with_commit_and_splits(cuda_lib):
+    """Batch 64 serving step with commit: pair and single-CTA kernels agree,
+    the commit is bit-exact, the tile counters are unchanged."""
+    import block_causal_paged_gb300 as bca
+    case = workloads.serving_decode(seed=5, D=64, keep_logical=False)
+    r = DecodeRun(case)
+    bca.workspace_init(r.ws)
+    got = r.run(commit=True).clone()
+    assert r.status() == 0
+    counts_pair = bca.read_tile_counters(r.ws)
+    kp_pair = r.k_pool.clone()
+    r2 = DecodeRun(case)
+    with single_cta_kernel():
+        bca.workspace_init(r2.ws)
+        one = r2.run(commit=True).clone()
+    assert r2.status() == 0
+    assert counts_pair == bca.read_tile_counters(r2.ws)
+    assert torch.equal(kp_pair.view(torch.int16), r2.k_pool.view(torch.int16))
+    diff = (got.double() - one.double()).abs()
+    assert float(diff.max()) <= 2e-2 and float(diff.mean()) <= 2e-3
+
+
+def test_pair_decode_repeated_launches_are_stable(cuda_lib):
+    """Twenty launches in a row on one workspace (work counter reset by the
+    last CTA, mailbox and barrier phases restart per launch): identical bits."""
+    case = workloads.make_decode_case([4096, 128, 20480, 640], D=64, Hq=32, Hkv=8, d=128,
+                                      seed=52, keep_logical=False)
+    r = DecodeRun(case)
+    first = r.run().clone()
+    for _ in range(19):
+        r.run()
+    assert r.status() == 0
+    assert torch.equal(first.view(torch.int16), r.out.view(torch.int16))
+
+
+@pytest.mark.parametrize("lens,D,Hq,Hkv", [
+    ([300, 512, 64, 1000], 64, 8, 2),       # ragged lengths, partial diagonal tiles
+    ([1024, 129], 16, 32, 8),               # D = 16
+    ([384, 77], 384, 6, 2),                 # G = 3: the last head pair has one head
+    ([2048], 128, 16, 8),                   # G = 2
+])
+def test_pair_prefill_matches_oracle_and_single_cta(cuda_lib, lens, D, Hq, Hkv):
+    case = workloads.make_prefill_case(lens, D=D, Hq=Hq, Hkv=Hkv, d=128, seed=53)
+    r = PrefillRun(case, write_pages=False)
+    got = r.run().clone()
+    assert r.status() == 0
+    ref = oracle.prefill(case.q, case.k, case.v, case.cu_seqlens, case.D)
+    assert_close(got, ref, what=f"pair prefill {lens} D={D}")
+    with single_cta_kernel():
+        one = r.run().clone()
+    assert r.status() == 0
+    diff = (got.double() - one.double()).abs()
+    assert float(diff.max()) <= 2e-2 and float(diff.mean()) <= 2e-3
