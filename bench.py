@@ -247,9 +247,11 @@ def run_reference(args):
 
 
 def kernel_source_hash():
+    """Hash of the sources of the decode step's attention kernel (the CTA-pair
+    kernel for the benchmarked shape) and what it includes."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("attention.cu", "ptx_sm103.cuh", "bca_internal.h"):
+    for f in ("attention_pair.cu", "attn_common.cuh", "ptx_sm103.cuh", "bca_internal.h"):
         with open(os.path.join(ROOT, "block_causal_paged_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -582,7 +584,7 @@ def run_ours(args):
     t_flop = alg["flops"] / (pk["bf16_tflops"] * 1e12)
     bound = "hbm" if t_mem >= t_flop else "tensor"
     roofline = {
-        "kernel": "attention (bca_decode main kernel)",
+        "kernel": "attention_pair_kernel (bca_decode main kernel: CTA pairs, tcgen05 cta_group::2)",
         "bound": bound,
         "achieved": achieved_gbs if bound == "hbm" else achieved_tflops,
         "peak": pk["hbm_gbs"] if bound == "hbm" else pk["bf16_tflops"],
