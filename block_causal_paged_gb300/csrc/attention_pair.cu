@@ -65,7 +65,7 @@ struct PCfg {
   static constexpr int kOffKV = kOffQ + kQBytes;
   static constexpr int kOffRec = kOffKV + kStages * kStageBytes;
   static constexpr int kTileSlots = 8;          // tile-full barriers (tiles in flight < 8)
-  static constexpr int kNumBars = 2 * kNumRec + kTileSlots + kStages + 10 + 2 * kMailSlots;
+  static constexpr int kNumBars = 2 * kNumRec + kTileSlots + kStages + 9 + 2 * kMailSlots;
   static constexpr int kOffBar = kOffRec + kNumRec * (int)sizeof(Rec);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM address, abort flag, mailbox
   static constexpr int kOffMl = kOffMisc + 64;              // merge exchange: float2 [2][128]
@@ -86,7 +86,6 @@ struct PBars {
   uint64_t* q_empty;
   uint64_t* s_full;     // [2] S buffer ready
   uint64_t* p_full;     // [2 S buffers] first CTA: P of both key halves written by both CTAs
-  uint64_t* pv_done;    // P V of a tile completed (both halves)
   uint64_t* o_full;
   uint64_t* o_empty;    // first CTA: both CTAs have read O
   uint64_t* drain;
@@ -301,7 +300,7 @@ __device__ __forceinline__ void run_mma(const PCtx& c, const AttnParams& p, int 
       tc_fence_after();
       issue_pv(c, buf, 0, vs, j > 0);
       issue_pv(c, buf, 1, vs, j > 0);
-      umma_commit_pair_mc(c.bar.pv_done, kBoth);
+      // (this commit also tells the softmax warps that O holds P V of tile j)
       umma_commit_pair_mc(&c.bar.kv_empty[vs], kBoth);
       if (nxt) {
         issue_qk(c, buf, ks);
@@ -407,10 +406,13 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O_h holds the P V of the earlier tiles; the last of them (this
-        // CTA's tile tc - 1) may still be running.  Its completion is phase
-        // tc - 1 of pv_done, and no later phase can have completed (P V of
-        // tile tc needs this warp's P).
-        if (!wait_bar_warp(c, p, c.bar.pv_done, (tc - 1u) & 1u)) return;
+        // CTA's tile tc - 1) may still be running.  The MMA warp frees the
+        // stage of V(tc - 1) (load 2 tc - 1) right after that P V, so its
+        // completion is that stage's phase; the stage's next phase needs the
+        // load 11 later consumed (Q K^T of tile tc + 5, after P of tile
+        // tc + 3), so no later phase can have completed.
+        const uint32_t lv = 2u * tc - 1u;
+        if (!wait_bar_warp(c, p, &c.bar.kv_empty[lv % C::kStages], (lv / C::kStages) & 1u)) return;
         tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < kHD; c0 += 32) {
@@ -546,13 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.bar.q_empty = c.bar.q_full + 1;
   c.bar.s_full = c.bar.q_empty + 1;
   c.bar.p_full = c.bar.s_full + 2;
-  c.bar.pv_done = c.bar.p_full + 2;
-  c.bar.o_full = c.bar.pv_done + 1;
+  c.bar.o_full = c.bar.p_full + 2;
   c.bar.o_empty = c.bar.o_full + 1;
   c.bar.drain = c.bar.o_empty + 1;
   c.bar.mail_full = c.bar.drain + 1;
   c.bar.mail_empty = c.bar.mail_full + kMailSlots;
-  static_assert(2 * kNumRec + C::kTileSlots + C::kStages + 10 + 2 * kMailSlots == C::kNumBars,
+  static_assert(2 * kNumRec + C::kTileSlots + C::kStages + 9 + 2 * kMailSlots == C::kNumBars,
                 "barriers");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   c.abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -576,7 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (S of the next tile is ready early), and its arrival must not complete
     // the phase of the tile the others are still on
     for (int b = 0; b < 2; ++b) mbar_init(&c.bar.p_full[b], 16);  // 8 warps of each CTA
-    mbar_init(c.bar.pv_done, 1);
     mbar_init(c.bar.o_full, 1);
     mbar_init(c.bar.o_empty, 16);      // 8 warps of each CTA
     mbar_init(c.bar.drain, 1);

@@ -109,3 +109,25 @@ def test_pair_prefill_matches_oracle_and_single_cta(cuda_lib, lens, D, Hq, Hkv):
     assert r.status() == 0
     diff = (got.double() - one.double()).abs()
     assert float(diff.max()) <= 2e-2 and float(diff.mean()) <= 2e-3
+
+
+@pytest.mark.parametrize("single", [False, True])
+def test_decode_with_growing_scores_rescales(cuda_lib, single):
+    """Keys scaled by 1 + 3t in prefix tile t: each new tile raises the row
+    maxima by far more than 2^8 (in exp2 units), so the online softmax
+    rescales O at most tiles (the rare path of both kernels), including
+    across split-KV chunks; outputs against the oracle."""
+    P = [2048, 4096, 640]
+    case = workloads.make_decode_case(P, D=64, Hq=32, Hkv=8, d=128, seed=57)
+    for b, Pb in enumerate(P):
+        f = (1.0 + 3.0 * (torch.arange(Pb) // 128)).to(torch.float32)[:, None, None]
+        case.k_prefix[b] = (case.k_prefix[b].float() * f).to(torch.bfloat16)
+        workloads.write_logical_into_pool(case.pool, b, case.k_prefix[b], case.v_prefix[b])
+    r = DecodeRun(case)
+    if single:
+        with single_cta_kernel():
+            got = r.run().clone()
+    else:
+        got = r.run().clone()
+    assert r.status() == 0
+    assert_close(got, _decode_ref(case), what=f"growing scores, single={single}")
