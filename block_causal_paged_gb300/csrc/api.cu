@@ -529,11 +529,9 @@ int decode_impl(const bca_dims* d, const void* q, const void* k_blk, const void*
   const long long max_items =
       (long long)d->batch * d->num_kv_heads * p.n_rb * ceil_div_i(max_tiles, kChMin);
   int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
-  // CTA pairs: decode blocks whose first row block fills both M-tiles, made
-  // of whole 16-key chunks (so every page box is whole), head_dim 128
+  // CTA pairs: blocks whose first row block fills both M-tiles, head_dim 128
   int n_pairs = 0;
-  if (pair_kernel_enabled() && HD == 128 && !causal && d->block_size % kChunkKeys == 0 &&
-      d->block_size > p.tpm) {
+  if (pair_kernel_enabled() && HD == 128 && d->block_size > p.tpm) {
     n_pairs = (int)std::min<long long>(pair_capacity(di.sms), std::max<long long>(1, max_items));
     p.pair = n_pairs > 0 ? 1 : 0;
   }
@@ -724,10 +722,20 @@ int multicanvas_impl(const bca_dims* d, const void* q_live, const void* k_live,
   const long long max_items =
       (long long)d->batch * d->num_kv_heads * ceil_div_i(max_live, 2 * p.tpm);
   const int grid = (int)std::min<long long>(di.sms, std::max<long long>(1, max_items));
+  // CTA pairs for head_dim 128 (items are two M-tiles of live rows)
+  int n_pairs = 0;
+  if (pair_kernel_enabled() && HD == 128) {
+    n_pairs = (int)std::min<long long>(pair_capacity(di.sms), std::max<long long>(1, max_items));
+    p.pair = n_pairs > 0 ? 1 : 0;
+  }
   cudaStream_t s = (cudaStream_t)stream;
-  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, grid, s); }) != cudaSuccess)
+  if (timed(BCA_KERNEL_PLAN, s, [&] { return launch_plan(p, p.pair ? n_pairs : grid, s); }) !=
+      cudaSuccess)
     return BCA_ERR_CUDA;
-  if (timed(BCA_KERNEL_ATTENTION, s, [&] { return launch_attention(p, maps, HD, grid, s); }) != cudaSuccess)
+  if (timed(BCA_KERNEL_ATTENTION, s, [&] {
+        return p.pair ? launch_attention_pair(p, maps, n_pairs, s)
+                      : launch_attention(p, maps, HD, grid, s);
+      }) != cudaSuccess)
     return BCA_ERR_CUDA;
   if (commit_rows && max_commit > 0) {
     PromoteParams c;

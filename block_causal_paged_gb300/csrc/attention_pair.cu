@@ -1,6 +1,7 @@
 // Block-causal attention on CTA pairs, sm_103a (tcgen05 cta_group::2 + TMA):
-// the decode step (a block of D >= 16 queries per sequence, a multiple of 16)
-// and the prefill, head_dim 128.
+// the decode step and short extend when their query rows fill two M-tiles,
+// the prefill and the multicanvas step (with or without the sliding-window
+// band), head_dim 128.
 //
 // A cluster of two CTAs on neighbouring SMs works on one item at a time.  An
 // item is up to 256 query rows sharing one KV head -- two M-tiles of 128 rows,
@@ -328,6 +329,9 @@ __device__ __forceinline__ void arrive_first(const PCtx& c, uint64_t* bar, uint3
   else mbar_arrive_remote_cta(bar0);
 }
 
+// kBand: the multicanvas sliding-window band (a per-row lower key bound), a
+// separate instantiation.
+template <bool kBand>
 __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, int h, int wq,
                                             int lane) {
   using C = PCfg;
@@ -347,7 +351,7 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
     const Rec* rec = ring_get(c, p, ri);
     if (!rec) return;
     const int kind = rec->w[I_KIND];
-    const int n_t = rec->w[I_NT];
+    const int n_t = rec->w[I_NT], qmode = rec->w[I_QMODE];
     const int qtok = rec->w[I_QTOK + m], qhead = rec->w[I_QHEAD + m];
     const int ntok = rec->w[I_NTOK + m], qbase = rec->w[I_QBASE + m];
     const int P0 = rec->w[I_P0], Dblk = rec->w[I_DBLK], split = rec->w[I_SPLIT];
@@ -356,14 +360,42 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
     if (kind == kRecEnd) return;
     const int tok = r / p.hpr;
     const bool valid = r < p.hpr * p.tpm && tok < ntok;
-    // row limit: keys at positions below lim are visible (INT_MAX for rows
-    // nobody stores, which then see every valid key)
-    const int lim = valid ? row_limit(qbase + tok, P0, Dblk) : INT_MAX;
+    // row q sees key positions in [lo, lim) (rows nobody stores see every
+    // valid key: lim = INT_MAX)
+    int lim = INT_MAX, lo = INT_MIN;
+    if (valid) {
+      const int qpos = qmode == 0 ? qbase + tok : __ldg(p.live_pos + qbase + tok);
+      lim = row_limit(qpos, P0, Dblk);
+      if (kBand) lo = qpos - p.window + 1;
+    }
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n_t; ++j) {
       const Rec* t = ring_get(c, p, ri);
       if (!t) return;
       const int full = t->w[T_FULL], nvalid = t->w[T_NVALID], kbase = t->w[T_KBASE];
+      const int kmode = t->w[T_KMODE];
+      // Stored positions (arena keys: kmode 1, 16 consecutive kv_pos entries
+      // per chunk from the chunk's offset; live keys: kmode 2, consecutive
+      // live_pos entries): lane l fetches keys 64h + 2l, 64h + 2l + 1 now,
+      // so that the load is in flight while S is computed; INT_MAX past the
+      // valid keys (never seen).
+      int kp0 = INT_MAX, kp1 = INT_MAX;
+      if (!full && kmode != 0) {
+        const int k0 = 64 * h + 2 * lane;
+        if (k0 < nvalid) {
+          const int32_t* src = kmode == 1
+                                   ? p.kv_pos + t->w[T_KOFF + k0 / kChunkKeys] + k0 % kChunkKeys
+                                   : p.live_pos + kbase + k0;
+          if (k0 + 2 <= nvalid && (reinterpret_cast<uintptr_t>(src) & 7) == 0) {
+            const int2 v2 = __ldg(reinterpret_cast<const int2*>(src));
+            kp0 = v2.x;
+            kp1 = v2.y;
+          } else {
+            kp0 = __ldg(src);
+            if (k0 + 1 < nvalid) kp1 = __ldg(src + 1);
+          }
+        }
+      }
       ring_release(c, ri, lane);
       ++ri;
       const uint32_t buf = tc & 1u;
@@ -374,13 +406,55 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
       tmem_ld64_sync(t_s + 128 * buf, sa, sb);
 #define SV(k) ((k) < 32 ? sa[(k)] : sb[(k) - 32])
       if (!full) {
-        // key 64h + k of the tile is visible iff it is one of the tile's
-        // valid keys and its position kbase + 64h + k is below the row's
-        // limit (lim >= 0 and kbase >= 0, so lim - kbase cannot overflow)
-        const int cut = max(0, min(64, min(nvalid, lim - kbase) - 64 * h));
+        if (kmode == 0) {
+          // key 64h + k is at position kbase + 64h + k: visible iff it is one
+          // of the tile's valid keys and in [lo, lim) (lim >= 0 and kbase >= 0,
+          // so lim - kbase cannot overflow; lo - kbase is clamped)
+          const int hi_cut = max(0, min(64, min(nvalid, lim - kbase) - 64 * h));
+          const int lo_cut =
+              kBand ? max(0, min(64, (int)max((long long)lo - kbase, -1ll) - 64 * h)) : 0;
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (k >= cut) SV(k) = __float_as_uint(-INFINITY);
+          for (int k = 0; k < 64; ++k)
+            if (k >= hi_cut || k < lo_cut) SV(k) = __float_as_uint(-INFINITY);
+        } else {
+          // visibility of key 64h + 2l + i for this row is bit l of vis[i]:
+          // rows with the same key range share one pair of ballots over the
+          // lanes' positions (a warp's rows: a few tokens of one or two
+          // canvases; with the band each token has its own lower bound)
+          uint32_t vis0 = 0u, vis1 = 0u;
+          bool done = !valid;  // rows past the item's tokens see nothing
+          while (true) {
+            const uint32_t pend = __ballot_sync(0xffffffffu, !done);
+            if (pend == 0u) break;
+            const int leader = __ffs(pend) - 1;
+            const int L = __shfl_sync(0xffffffffu, lim, leader);
+            const int Lo = kBand ? __shfl_sync(0xffffffffu, lo, leader) : INT_MIN;
+            const uint32_t b0 = __ballot_sync(0xffffffffu, kBand ? (kp0 < L && kp0 >= Lo) : kp0 < L);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, kBand ? (kp1 < L && kp1 >= Lo) : kp1 < L);
+            if (!done && lim == L && (!kBand || lo == Lo)) {
+              vis0 = b0;
+              vis1 = b1;
+              done = true;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (!((((k & 1) ? vis1 : vis0) >> (k >> 1)) & 1u)) SV(k) = __float_as_uint(-INFINITY);
+        }
+        // V rows past the valid keys inside the last partly valid 16-key
+        // chunk came in with its box and may hold anything (a pool page's
+        // unused slots, another buffer's rows): their P is 0, but 0 * NaN is
+        // NaN in P V, so warpgroup 0 zeroes them in this CTA's V stage
+        // before P is published
+        if (h == 0 && (nvalid & (kChunkKeys - 1)) != 0) {
+          const int n_zero = kChunkKeys - (nvalid & (kChunkKeys - 1));
+          const uint32_t vrow0 =
+              smem_u32(c.smem + C::kOffKV + ((2u * tc + 1u) % C::kStages) * C::kStageBytes) +
+              (uint32_t)nvalid * 128u;
+          for (int i = r; i < n_zero * 8; i += 128)
+            st_shared_v4(vrow0 + (uint32_t)i * 16u, 0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
       }
       // row maximum of the raw scores (the scale is positive), in log2 units
       float mx[4] = {__uint_as_float(SV(0)), __uint_as_float(SV(1)), __uint_as_float(SV(2)),
@@ -522,6 +596,7 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
 // ============================================================================
 // the kernel
 // ============================================================================
+template <bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_kp,
@@ -624,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_alloc<kRegsSoftmax>();
     named_barrier_sync(1, kThreads);
-    run_softmax(c, p, (warp - 4) >> 2, warp & 3, lane);
+    run_softmax<kBand>(c, p, (warp - 4) >> 2, warp & 3, lane);
     __syncwarp();
     regs_dealloc<kRegsLaunch>();
   }
@@ -651,8 +726,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_attention_pair(const AttnParams& p, const AttnMaps& maps, int n_pairs,
-                                  cudaStream_t stream) {
+namespace {
+template <bool kBand>
+cudaError_t launch_pair(const AttnParams& p, const AttnMaps& maps, int n_pairs,
+                        cudaStream_t stream) {
   using C = PCfg;
   static std::atomic<bool> configured[kMaxDevices];
   int dev = 0;
@@ -660,11 +737,13 @@ cudaError_t launch_attention_pair(const AttnParams& p, const AttnMaps& maps, int
   if (e != cudaSuccess) return e;
   const bool cached = dev >= 0 && dev < kMaxDevices;
   if (!cached || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(attention_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemAlloc);
+    e = cudaFuncSetAttribute(attention_pair_kernel<kBand>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits for registers released by setmaxnreg.dec; the
+    // split must fit what the block is launched with
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attention_pair_kernel);
+    e = cudaFuncGetAttributes(&fa, attention_pair_kernel<kBand>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
     if (cached) configured[dev].store(true, std::memory_order_release);
@@ -683,16 +762,24 @@ cudaError_t launch_attention_pair(const AttnParams& p, const AttnMaps& maps, int
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attention_pair_kernel, maps.q, maps.kp, maps.vp, maps.kd,
+  return cudaLaunchKernelEx(&cfg, attention_pair_kernel<kBand>, maps.q, maps.kp, maps.vp, maps.kd,
                             maps.vd, p);
+}
+}  // namespace
+
+cudaError_t launch_attention_pair(const AttnParams& p, const AttnMaps& maps, int n_pairs,
+                                  cudaStream_t stream) {
+  const bool band = p.mode == kModeMulticanvas && p.window > 0;
+  return band ? launch_pair<true>(p, maps, n_pairs, stream)
+              : launch_pair<false>(p, maps, n_pairs, stream);
 }
 
 int attention_pair_max_pairs(int n_sms) {
   using C = PCfg;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaFuncSetAttribute(attention_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemAlloc) != cudaSuccess)
+  if (cudaFuncSetAttribute(attention_pair_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (n_sms / 2));
@@ -706,7 +793,8 @@ int attention_pair_max_pairs(int n_sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attention_pair_kernel, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attention_pair_kernel<false>, &cfg) != cudaSuccess)
+    return 0;
   return n;
 }
 

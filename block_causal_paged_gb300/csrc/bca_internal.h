@@ -116,9 +116,9 @@ cudaError_t launch_plan(const AttnParams& p, int attn_grid, cudaStream_t stream)
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& maps, int head_dim, int grid,
                              cudaStream_t stream);
 
-// Launch the CTA-pair attention kernel (decode with D a multiple of 16 and at
-// least two M-tiles per item, or prefill; head_dim 128) on n_pairs clusters of
-// two CTAs.
+// Launch the CTA-pair attention kernel (decode or extend with two M-tiles in
+// the first row block, prefill, multicanvas; head_dim 128) on n_pairs
+// clusters of two CTAs.
 cudaError_t launch_attention_pair(const AttnParams& p, const AttnMaps& maps, int n_pairs,
                                   cudaStream_t stream);
 // Clusters of two CTAs of that kernel that can be resident at once (0 on error).

@@ -131,3 +131,51 @@ def test_decode_with_growing_scores_rescales(cuda_lib, single):
         got = r.run().clone()
     assert r.status() == 0
     assert_close(got, _decode_ref(case), what=f"growing scores, single={single}")
+
+
+def _mc_ref(c, window=0):
+    return oracle.multicanvas(c.q_live, c.k_live, c.v_live, c.live_pos, c.live_count, c.arena_k,
+                              c.arena_v, c.arena_pos, c.prompt_len, c.canvas_len, window=window)
+
+
+@pytest.mark.parametrize("args,window,shuffle", [
+    ((4, 1024, 3, 256, 32, 8, 128), 0, False),    # the 3-canvas step (prompt 1024)
+    ((3, 300, 4, 96, 16, 4, 128), 0, True),       # ragged arena and prompt, shuffled live rows
+    ((4, 1024, 5, 256, 32, 8, 128), 1024, False),  # 5 canvases under a 1024-token window
+    ((2, 100, 3, 64, 32, 8, 128), 50, True),       # a narrow band, shuffled live rows
+])
+def test_pair_multicanvas_matches_oracle_and_single_cta(cuda_lib, args, window, shuffle):
+    """The multicanvas step on CTA pairs: key masks from stored positions
+    (arena kv_pos, live_pos), the band, ragged arena chunks whose unused pool
+    slots hold NaN; live rows against the oracle and the single-CTA kernel."""
+    from _gpu_cases import MulticanvasRun
+    c = workloads.make_multicanvas_case(*args, seed=61, shuffle_live=shuffle)
+    m = torch.from_numpy(np.arange(c.q_live.shape[1])[None, :] < c.live_count.numpy()[:, None])
+    r = MulticanvasRun(c, promote=False)
+    got = r.run(window=window).cpu().clone()
+    assert r.status() == 0
+    ref = _mc_ref(c, window)
+    assert_close(got[m], ref[m.numpy()], what=f"pair multicanvas {args} window {window}")
+    with single_cta_kernel():
+        one = MulticanvasRun(c, promote=False).run(window=window).cpu()
+    diff = (got[m].double() - one[m].double()).abs()
+    assert float(diff.max()) <= 2e-2 and float(diff.mean()) <= 2e-3
+
+
+@pytest.mark.parametrize("P,D", [([5, 77, 1000, 33], 48), ([129, 3000], 72)])
+def test_pair_decode_ragged_chunks(cuda_lib, P, D):
+    """Blocks and prefixes that are not whole 16-key chunks on CTA pairs (the
+    extend's causal mask, and a block decode after prefixes that are multiples
+    of D but not of 16): the ragged V rows, NaN in the pool, are zeroed."""
+    case = workloads.make_decode_case(P, D=D, Hq=32, Hkv=8, d=128, seed=63)
+    r = DecodeRun(case)
+    got = r.run(extend=True).clone()
+    assert r.status() == 0
+    ref = oracle.extend(case.q, case.k_blk, case.v_blk, case.k_prefix, case.v_prefix)
+    assert_close(got, ref, what=f"pair extend P={P} D={D}")
+    Pd = [p_ // D * D for p_ in P]
+    cd = workloads.make_decode_case(Pd, D=D, Hq=32, Hkv=8, d=128, seed=64)
+    rd = DecodeRun(cd)
+    gd = rd.run().clone()
+    assert rd.status() == 0
+    assert_close(gd, _decode_ref(cd), what=f"pair decode P={Pd} D={D}")
