@@ -30,6 +30,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode-step attention µs, TFLOP/s, HBM GB/s and % of roofline at B=64"
+# device cycles (about 100 us) of busy-waiting queued before each row call, so
+# that the events around the call time device work, not host marshalling
+HOST_LEAD_CYCLES = 200_000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
@@ -337,7 +340,7 @@ def prefill_row(args, bca, workloads, torch, dev, roof, time_calls, reps, res):
     pairs = sum(c.D * c.D * (L // c.D) * (L // c.D + 1) // 2 for L in c.seq_lens)
     flops = 4.0 * c.d * c.Hq * pairs
     bytes_ = T * (2 * c.Hq + 2 * c.Hkv) * c.d * 2.0 + 2 * T * c.Hkv * c.d * 2.0
-    res["prefill"] = dict(roof(flops, bytes_, ms), workload="4 x 8192 tokens, D=64, 32/8 heads, "
+    res["prefill"] = dict(roof(flops, bytes_, ms), kernel_us=dict(time_calls.kernel_us), workload="4 x 8192 tokens, D=64, 32/8 heads, "
                           "d=128, K/V written to pages of 16")
     del q, k, v, out, kp, vp, ws
 
@@ -368,9 +371,12 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
                 "frac": max(t_mem, t_flop) / (ms * 1e-3),
                 "algorithmic_flops": flops, "algorithmic_bytes": bytes_}
 
-    # every timed call starts with a cold L2: a buffer of twice the L2 size is
-    # rewritten before it (outside the events)
+    # every timed call starts with a cold, clean L2 (outside the events): a
+    # buffer of twice the L2 size is rewritten, then another one is read, so
+    # that the L2 holds none of the call's data and no dirty lines whose
+    # write-back the call would pay for
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(64 << 20, dtype=torch.int32, device=dev)
 
     def time_calls(fn, n):
         for _ in range(3):
@@ -378,12 +384,21 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         torch.cuda.synchronize()
+        bca.profile_start(16 * n + 16)
         for a, b in evs:
             flush.fill_(1)
+            flush_rd.sum()
+            # keep the device busy while the host marshals the call, so that
+            # the events bracket device work and no host time
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
             a.record(stream)
             fn()
             b.record(stream)
         torch.cuda.synchronize()
+        prof = bca.profile_stop()
+        # per kernel kind, the mean device time of its launches (the library's
+        # own event pairs around each launch)
+        time_calls.kernel_us = {k: 1e3 * ms / cnt for k, (cnt, ms) in prof.items() if cnt}
         return statistics.median(a.elapsed_time(b) for a, b in evs)
 
     # prefill: 4 sequences of 8192 tokens, D = 64, 32/8 heads, d = 128, pages written
@@ -418,7 +433,7 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         A = int(case.arena_len.sum())
         nl = int(case.live_count.sum())
         bytes2 = (A + nl) * case.Hkv * case.d * 2 * 2.0 + 2 * nl * case.Hq * case.d * 2.0
-        res[name] = dict(roof(flops2, bytes2, ms2), workload=desc)
+        res[name] = dict(roof(flops2, bytes2, ms2), workload=desc, kernel_us=dict(time_calls.kernel_us))
 
     if want("qkv_post"):
         # QKV-post: batch 64 blocks of 64 tokens after the serving prefixes,
@@ -444,7 +459,7 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         tokens = cq.B * cq.n
         row = (cq.Hq + 2 * cq.Hkv) * cq.d * 2.0
         bytes_q = tokens * (2 * row + 2 * cq.Hkv * cq.d * 2.0 + 8.0) + 2 * cq.d * 2.0
-        res["qkv_post"] = dict(roof(0.0, bytes_q, ms_q),
+        res["qkv_post"] = dict(roof(0.0, bytes_q, ms_q), kernel_us=dict(time_calls.kernel_us),
                                workload=f"batch {cq.B} x 64 tokens after the serving prefixes, 32/8 heads, "
                                         "d=128: per-head RMS norms + RoPE (theta 1e6) of q and k, "
                                         "K/V rows written to pages of 16")
@@ -472,7 +487,7 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         kv_row = 2 * ce.Hkv * ce.d * 2.0  # K and V bytes of one token
         bytes_e = (sum(P) * kv_row + ce.B * n * (2 * ce.Hq * ce.d * 2.0 + 2 * kv_row)
                    + ce.B * ce.pool.max_pages_per_seq * 4.0)
-        res["extend"] = dict(roof(flops_e, bytes_e, ms_e),
+        res["extend"] = dict(roof(flops_e, bytes_e, ms_e), kernel_us=dict(time_calls.kernel_us),
                              workload=f"batch {ce.B}, 9 new causal tokens after log-uniform prefixes in "
                                       f"[128, 32768] (sum {sum(P)}), 32/8 heads, d=128, page 16, "
                                       f"new rows committed")

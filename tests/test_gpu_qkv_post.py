@@ -152,3 +152,28 @@ def test_small_rows_where_epsilon_matters(cuda_lib, scale, eps):
     g = r.q.float().cpu().numpy().astype(np.float64)
     bound = 2.0 ** -8 * np.abs(q0) + 2.0 ** -16
     assert (np.abs(g - q0) > bound).mean() > 0.5
+
+
+def test_long_token_ranges_per_sm(cuda_lib):
+    """65536 tokens (8 x 8192) of 2/1 heads, d = 64: every SM's share runs to
+    hundreds of tokens, so each consumer warp reloads its window of token
+    metadata several times; rows of 4 heads leave a partial work unit per
+    token.  Outputs against the oracle, the cache writes and kv_pos
+    (arena mode) bit-exact."""
+    c = workloads.make_qkv_post_case(8, 8192, 2, 1, 64, prefix_len=[0, 64, 128, 0, 512, 64, 0, 1024],
+                                     seed=11)
+    r = Run(c)
+    r.run(arena=True)
+    assert r.status() == 0
+    _check(r)
+    S = c.pool.page_size
+    wp = c.write_pos.long()
+    pages = torch.gather(c.pool.page_table.long(), 1, wp // S)
+    kp, vp = c.pool.k_pool.clone(), c.pool.v_pool.clone()
+    kv_pos = torch.full((c.pool.num_pages, S), -7, dtype=torch.int32)
+    kp[pages.flatten(), :, (wp % S).flatten()] = r.k.cpu().reshape(-1, c.Hkv, c.d)
+    vp[pages.flatten(), :, (wp % S).flatten()] = r.v.cpu().reshape(-1, c.Hkv, c.d)
+    kv_pos[pages.flatten(), (wp % S).flatten()] = c.positions.flatten().int()
+    assert torch.equal(r.k_pool.cpu().view(torch.int16), kp.view(torch.int16))
+    assert torch.equal(r.v_pool.cpu().view(torch.int16), vp.view(torch.int16))
+    assert torch.equal(r.kv_pos.cpu(), kv_pos)
