@@ -342,6 +342,10 @@ def prefill_row(args, bca, workloads, torch, dev, roof, time_calls, reps, res):
     bytes_ = T * (2 * c.Hq + 2 * c.Hkv) * c.d * 2.0 + 2 * T * c.Hkv * c.d * 2.0
     res["prefill"] = dict(roof(flops, bytes_, ms), kernel_us=dict(time_calls.kernel_us), workload="4 x 8192 tokens, D=64, 32/8 heads, "
                           "d=128, K/V written to pages of 16")
+    ku = time_calls.kernel_us.get("attention")
+    if ku:  # the attention kernel alone (the library's own events around each launch)
+        k = roof(flops, bytes_, ku * 1e-3)
+        res["prefill"]["kernel"] = {"name": "attention", "us": ku, "frac": k["frac"], "bound": k["bound"]}
     del q, k, v, out, kp, vp, ws
 
 
@@ -361,6 +365,15 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
 
     def reps(n):
         return args.row_reps if args.row_reps else n
+
+    def with_kernel(row, flops, bytes_, name):
+        """Adds the figure of the row's dominant kernel (the library's own
+        events around each launch) for the same algorithmic work."""
+        ku = time_calls.kernel_us.get(name)
+        if ku:
+            k = roof(flops, bytes_, ku * 1e-3)
+            row["kernel"] = {"name": name, "us": ku, "frac": k["frac"], "bound": k["bound"]}
+        return row
 
     def roof(flops, bytes_, ms):
         t_mem = bytes_ / (pk["hbm_gbs"] * 1e9)
@@ -433,7 +446,8 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         A = int(case.arena_len.sum())
         nl = int(case.live_count.sum())
         bytes2 = (A + nl) * case.Hkv * case.d * 2 * 2.0 + 2 * nl * case.Hq * case.d * 2.0
-        res[name] = dict(roof(flops2, bytes2, ms2), workload=desc, kernel_us=dict(time_calls.kernel_us))
+        res[name] = with_kernel(dict(roof(flops2, bytes2, ms2), workload=desc,
+                                     kernel_us=dict(time_calls.kernel_us)), flops2, bytes2, "attention")
 
     if want("qkv_post"):
         # QKV-post: batch 64 blocks of 64 tokens after the serving prefixes,
@@ -459,10 +473,11 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         tokens = cq.B * cq.n
         row = (cq.Hq + 2 * cq.Hkv) * cq.d * 2.0
         bytes_q = tokens * (2 * row + 2 * cq.Hkv * cq.d * 2.0 + 8.0) + 2 * cq.d * 2.0
-        res["qkv_post"] = dict(roof(0.0, bytes_q, ms_q), kernel_us=dict(time_calls.kernel_us),
-                               workload=f"batch {cq.B} x 64 tokens after the serving prefixes, 32/8 heads, "
-                                        "d=128: per-head RMS norms + RoPE (theta 1e6) of q and k, "
-                                        "K/V rows written to pages of 16")
+        res["qkv_post"] = with_kernel(
+            dict(roof(0.0, bytes_q, ms_q), kernel_us=dict(time_calls.kernel_us),
+                 workload=f"batch {cq.B} x 64 tokens after the serving prefixes, 32/8 heads, "
+                          "d=128: per-head RMS norms + RoPE (theta 1e6) of q and k, "
+                          "K/V rows written to pages of 16"), 0.0, bytes_q, "qkv_post")
         del tq, oq, ok_, ov, wq, cq
 
     if want("extend"):
@@ -487,10 +502,11 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
         kv_row = 2 * ce.Hkv * ce.d * 2.0  # K and V bytes of one token
         bytes_e = (sum(P) * kv_row + ce.B * n * (2 * ce.Hq * ce.d * 2.0 + 2 * kv_row)
                    + ce.B * ce.pool.max_pages_per_seq * 4.0)
-        res["extend"] = dict(roof(flops_e, bytes_e, ms_e), kernel_us=dict(time_calls.kernel_us),
-                             workload=f"batch {ce.B}, 9 new causal tokens after log-uniform prefixes in "
-                                      f"[128, 32768] (sum {sum(P)}), 32/8 heads, d=128, page 16, "
-                                      f"new rows committed")
+        res["extend"] = with_kernel(
+            dict(roof(flops_e, bytes_e, ms_e), kernel_us=dict(time_calls.kernel_us),
+                 workload=f"batch {ce.B}, 9 new causal tokens after log-uniform prefixes in "
+                          f"[128, 32768] (sum {sum(P)}), 32/8 heads, d=128, page 16, "
+                          f"new rows committed"), flops_e, bytes_e, "attention")
         del te, oe, we, ce
 
     if want("multicanvas"):
