@@ -554,7 +554,9 @@ struct Planner {
     return p.live_pos ? __ldg(p.live_pos + (size_t)b * p.max_live + r) : p.prompt_len + r;
   }
 
-  // Multicanvas items: index space (row block, sequence, KV head).
+  // Multicanvas items: index space (sequence, KV head, row block), row
+  // blocks innermost, so that the items running at once share the keys of a
+  // few (sequence, KV head) groups and their tiles are read from L2.
   __device__ void run_multicanvas() {
     const int rows_per_item = 2 * p.tpm;
     const int n_items = p.n_rb_max * p.B * p.Hkv;
@@ -562,8 +564,8 @@ struct Planner {
     while (ok) {
       const int idx = grab();
       if (idx >= n_items) break;
-      const int rb = idx / (p.B * p.Hkv);
-      const int b = (idx / p.Hkv) % p.B, g = idx % p.Hkv;
+      const int rb = idx % p.n_rb_max;
+      const int b = idx / (p.n_rb_max * p.Hkv), g = (idx / p.n_rb_max) % p.Hkv;
       int n_live = p.lens ? __ldg(p.lens + b) : p.max_live;
       int A = __ldg(p.arena_len + b);
       if (n_live < 0 || n_live > p.max_live || A < 0 ||
