@@ -368,6 +368,14 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
       lim = row_limit(qpos, P0, Dblk);
       if (kBand) lo = qpos - p.window + 1;
     }
+    // band: the range of the warp's lower bounds [lo_min, lo_max] (rows that
+    // store nothing excluded); only keys with positions inside it can be
+    // seen by some of the warp's rows and not by others
+    int lo_min = INT_MAX, lo_max = INT_MIN;
+    if (kBand) {
+      lo_min = warp_min(valid ? lo : INT_MAX);
+      lo_max = warp_max(valid ? lo : INT_MIN);
+    }
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n_t; ++j) {
       const Rec* t = ring_get(c, p, ri);
@@ -418,9 +426,9 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
             if (k >= hi_cut || k < lo_cut) SV(k) = __float_as_uint(-INFINITY);
         } else {
           // visibility of key 64h + 2l + i for this row is bit l of vis[i]:
-          // rows with the same key range share one pair of ballots over the
+          // rows with the same upper limit share one pair of ballots over the
           // lanes' positions (a warp's rows: a few tokens of one or two
-          // canvases; with the band each token has its own lower bound)
+          // canvases)
           uint32_t vis0 = 0u, vis1 = 0u;
           bool done = !valid;  // rows past the item's tokens see nothing
           while (true) {
@@ -428,14 +436,35 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
             if (pend == 0u) break;
             const int leader = __ffs(pend) - 1;
             const int L = __shfl_sync(0xffffffffu, lim, leader);
-            const int Lo = kBand ? __shfl_sync(0xffffffffu, lo, leader) : INT_MIN;
-            const uint32_t b0 = __ballot_sync(0xffffffffu, kBand ? (kp0 < L && kp0 >= Lo) : kp0 < L);
-            const uint32_t b1 = __ballot_sync(0xffffffffu, kBand ? (kp1 < L && kp1 >= Lo) : kp1 < L);
-            if (!done && lim == L && (!kBand || lo == Lo)) {
+            const uint32_t b0 = __ballot_sync(0xffffffffu, kp0 < L);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, kp1 < L);
+            if (!done && lim == L) {
               vis0 = b0;
               vis1 = b1;
               done = true;
             }
+          }
+          if (kBand) {
+            // with the band each token has its own lower bound: keys at or
+            // above the warp's largest bound pass every row's, keys below
+            // its smallest pass none, and the few in between are tested one
+            // by one against this row's bound
+            uint32_t m0 = __ballot_sync(0xffffffffu, kp0 >= lo_max);
+            uint32_t m1 = __ballot_sync(0xffffffffu, kp1 >= lo_max);
+            uint32_t a0 = __ballot_sync(0xffffffffu, kp0 >= lo_min && kp0 < lo_max);
+            uint32_t a1 = __ballot_sync(0xffffffffu, kp1 >= lo_min && kp1 < lo_max);
+            while (a0 != 0u) {
+              const int l = __ffs(a0) - 1;
+              if (__shfl_sync(0xffffffffu, kp0, l) >= lo) m0 |= 1u << l;
+              a0 &= a0 - 1u;
+            }
+            while (a1 != 0u) {
+              const int l = __ffs(a1) - 1;
+              if (__shfl_sync(0xffffffffu, kp1, l) >= lo) m1 |= 1u << l;
+              a1 &= a1 - 1u;
+            }
+            vis0 &= m0;
+            vis1 &= m1;
           }
 #pragma unroll
           for (int k = 0; k < 64; ++k)
