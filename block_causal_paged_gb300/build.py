@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libbca.so")
 SOURCES = ["api.cu", "attention.cu", "attention_pair.cu", "kv_write.cu", "plan.cu", "static_scratch.cu", "combine.cu",
-           "confidence.cu", "qkv_post.cu"]
+           "confidence.cu", "qkv_post.cu", "debug_check.cu"]
 HEADERS = ["bca_internal.h", "ptx_sm103.cuh", "attn_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

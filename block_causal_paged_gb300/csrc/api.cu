@@ -360,6 +360,9 @@ int bca_qkv_post(const bca_dims* d, const void* qkv, const int32_t* positions,
       (write_pos && (!aligned16(k_pool) || !aligned16(v_pool))) || !aligned16(ws))
     return BCA_ERR_ALIGN;
   if (ws_bytes < kWsHeaderBytes) return BCA_ERR_WORKSPACE;
+  if (debug_enabled() &&
+      (rc = debug_check_qkv_post(d, write_pos, page_table, (cudaStream_t)stream)))
+    return rc;
   DeviceInfo di;
   if ((rc = device_info(&di))) return rc;
   QkvPostParams c;
@@ -436,6 +439,9 @@ int bca_commit_kv(const bca_dims* d, const void* k_blk, const void* v_blk, void*
       !aligned16(ws))
     return BCA_ERR_ALIGN;
   if (ws_bytes < kWsHeaderBytes) return BCA_ERR_WORKSPACE;
+  if (debug_enabled() &&
+      (rc = debug_check_commit(d, page_table, start_pos, num_tokens, (cudaStream_t)stream)))
+    return rc;
   CommitParams c;
   std::memset(&c, 0, sizeof(c));
   c.k_src = (const uint16_t*)k_blk;
@@ -480,6 +486,9 @@ int decode_impl(const bca_dims* d, const void* q, const void* k_blk, const void*
   const long long q_tokens = (long long)d->batch * d->block_size;
   if (q_tokens * d->num_q_heads >= (1ll << 31)) return BCA_ERR_INVALID_ARG;
   if (ws_bytes < kWsHeaderBytes + round_up((size_t)d->batch * 4, 256)) return BCA_ERR_WORKSPACE;
+  if (debug_enabled() &&
+      (rc = debug_check_decode(d, page_table, prefix_len, commit, causal, (cudaStream_t)stream)))
+    return rc;
   DeviceInfo di;
   if ((rc = device_info(&di))) return rc;
   const int G0 = d->num_q_heads / d->num_kv_heads;
@@ -588,6 +597,10 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
   if (k_pool && (long long)max_seqlen > (long long)d->max_pages_per_seq * d->page_size)
     return BCA_ERR_CAPACITY;
   if (ws_bytes < kWsHeaderBytes) return BCA_ERR_WORKSPACE;
+  if (debug_enabled() &&
+      (rc = debug_check_prefill(d, cu_seqlens, total_tokens, max_seqlen,
+                                k_pool ? page_table : nullptr, (cudaStream_t)stream)))
+    return rc;
   DeviceInfo di;
   if ((rc = device_info(&di))) return rc;
 
@@ -681,6 +694,10 @@ int multicanvas_impl(const bca_dims* d, const void* q_live, const void* k_live,
   if (q_tokens * d->num_q_heads >= (1ll << 31)) return BCA_ERR_INVALID_ARG;
   if (ws_bytes < multicanvas_ws_bytes(d->batch, d->max_pages_per_seq, d->page_size))
     return BCA_ERR_WORKSPACE;
+  if (debug_enabled() &&
+      (rc = debug_check_multicanvas(d, live_count, max_live, page_table, arena_len, commit_rows,
+                                    commit_count, max_commit, (cudaStream_t)stream)))
+    return rc;
   DeviceInfo di;
   if ((rc = device_info(&di))) return rc;
 

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+struct bca_dims;  // the public call dimensions (bca.h)
+
 namespace bca {
 
 constexpr int kTileKeys = 128;    // keys per KV tile
@@ -194,5 +196,22 @@ struct PromoteParams {
   WsHeader* hdr;
 };
 cudaError_t launch_promote(const PromoteParams& c, cudaStream_t stream);
+
+// Host-side input checks for BCA_DEBUG=1 (debug_check.cu): lengths,
+// positions and page-table entries copied to the host and checked before a
+// launch; BCA_OK or the error the entry point returns.
+bool debug_enabled();
+int debug_check_decode(const bca_dims* d, const int32_t* page_table,
+                       const int32_t* prefix_len, int commit, int causal, cudaStream_t s);
+int debug_check_prefill(const bca_dims* d, const int32_t* cu_seqlens, int32_t total_tokens,
+                        int32_t max_seqlen, const int32_t* page_table, cudaStream_t s);
+int debug_check_commit(const bca_dims* d, const int32_t* page_table,
+                       const int32_t* start_pos, int32_t num_tokens, cudaStream_t s);
+int debug_check_qkv_post(const bca_dims* d, const int32_t* write_pos,
+                         const int32_t* page_table, cudaStream_t s);
+int debug_check_multicanvas(const bca_dims* d, const int32_t* live_count, int32_t max_live,
+                            const int32_t* page_table, const int32_t* arena_len,
+                            const int32_t* commit_rows, const int32_t* commit_count,
+                            int32_t max_commit, cudaStream_t s);
 
 }  // namespace bca

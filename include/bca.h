@@ -85,6 +85,33 @@ extern "C" {
 #define BCA_ERR_DEVICE_BAD_LENGTH (-17) /* a length/position outside its range */
 #define BCA_ERR_DEVICE_TIMEOUT (-18)  /* an internal wait gave up (never expected) */
 
+/*
+ * Debug checks.  With the environment variable BCA_DEBUG=1 (read at each
+ * call), every entry point that takes lengths, positions or a page table
+ * copies them to the host (on the call's stream, waiting for the copy) and
+ * checks them before launching anything; a request that fails is refused
+ * and nothing runs:
+ *   BCA_ERR_INVALID_ARG  a length or position out of range for the call (a
+ *                        negative prefix, a decode prefix that is not a
+ *                        whole number of blocks, cu_seqlens not starting at
+ *                        0 / decreasing / not ending at total_tokens / a
+ *                        sequence longer than max_seqlen, two tokens of one
+ *                        QKV-post writing the same cache slot, a live row
+ *                        promoted twice or out of range, live_count above
+ *                        max_live);
+ *   BCA_ERR_CAPACITY     a range that runs past the sequence's page list;
+ *   BCA_ERR_PAGE_RANGE   a page-table entry the call uses outside
+ *                        [0, num_pages);
+ *   BCA_ERR_PAGE_SHARED  a page the call writes that another sequence also
+ *                        uses, or one page twice among one sequence's used
+ *                        entries (pages that several sequences only read,
+ *                        a shared prefix, are allowed).
+ * Without the variable these conditions are found on the device (a page id
+ * outside the pool or a position past the page list is skipped and reported
+ * through the status word; shared pages are not checked).  Not meant for a
+ * timed path: the copies synchronise the stream.
+ */
+
 /* Operations, for bca_workspace_size. */
 #define BCA_OP_DECODE 1
 #define BCA_OP_PREFILL 2

@@ -3,6 +3,7 @@ import numpy as np
 import pytest
 import torch
 
+import block_causal_paged_gb300 as bca
 import oracle
 import workloads
 from _gpu_cases import DecodeRun, assert_close
@@ -224,3 +225,22 @@ def test_decode_on_every_visible_device(cuda_lib):
             out = r.run()
             assert r.status() == 0
             assert_close(out, ref, what=f"device {dev}")
+
+
+def test_debug_checks_on_device_tables(cuda_lib, monkeypatch):
+    """BCA_DEBUG=1 with device-resident lengths and page table: a valid
+    decode runs and matches the oracle; a used page-table entry outside the
+    pool is refused on the host before any launch (the output buffer keeps
+    its contents), where without the switch the device would skip it."""
+    monkeypatch.setenv("BCA_DEBUG", "1")
+    case = workloads.make_decode_case([128, 4096, 64 * 7], D=64, Hq=8, Hkv=2, d=128, seed=12)
+    r = DecodeRun(case)
+    out = r.run(commit=True).clone()
+    assert r.status() == 0
+    assert_close(out, _ref(case), what="decode under BCA_DEBUG=1")
+    r.out.fill_(7.0)
+    r.page_table[1, 5] = case.pool.num_pages
+    with pytest.raises(bca.BcaError) as e:
+        r.run()
+    assert e.value.code == bca.ERR_PAGE_RANGE
+    assert bool((r.out == 7.0).all())
