@@ -351,7 +351,8 @@ def prefill_row(args, bca, workloads, torch, dev, roof, time_calls, reps, res):
 
 def other_rows(args, bca, workloads, torch, pk, dev, stream):
     """The block-causal prefill (4 x 8192), the QKV-post of a decode step's
-    blocks, the short causal extend (batch 64, 9 tokens) and the multicanvas step (batch 16, prompt 1024, 3 canvases of
+    blocks, the block decode at batch 8 (prefixes 512-4096), the short causal
+    extend (batch 64, 9 tokens) and the multicanvas step (batch 16, prompt 1024, 3 canvases of
     256; and 5 canvases under a 1024-token sliding window), each timed over repeated calls with CUDA events and set against
     its roofline: algorithmic flops (every visible (query, key) pair costs 4d
     per query head) and bytes (every input byte once, the output, page
@@ -479,6 +480,32 @@ def other_rows(args, bca, workloads, torch, pk, dev, stream):
                           "d=128: per-head RMS norms + RoPE (theta 1e6) of q and k, "
                           "K/V rows written to pages of 16"), 0.0, bytes_q, "qkv_post")
         del tq, oq, ok_, ov, wq, cq
+
+    if want("block_decode"):
+        # block decode: batch 8, 64-token blocks after prefixes uniform in
+        # {512, 576, ..., 4096}, 32/8 heads, d = 128 (K/V ~ 75 MB: L2-sized,
+        # hence the flush before every call)
+        cb = workloads.block_decode(seed=args.seed, keep_logical=False)
+        db = bca.dims(cb.B, cb.D, cb.Hq, cb.Hkv, cb.d, cb.pool.page_size, cb.pool.num_pages,
+                      cb.pool.max_pages_per_seq)
+        tb = {"q": cb.q.to(dev), "k": cb.k_blk.to(dev), "v": cb.v_blk.to(dev),
+              "kp": cb.pool.k_pool.to(dev), "vp": cb.pool.v_pool.to(dev),
+              "pt": cb.pool.page_table.to(dev),
+              "pl": torch.tensor(cb.prefix_len, dtype=torch.int32, device=dev)}
+        ob = torch.empty_like(tb["q"])
+        wb = bca.new_workspace(db, bca.OP_DECODE, device=dev)
+        ms_b = time_calls(lambda: bca.bca_decode(db, tb["q"], tb["k"], tb["v"], tb["kp"], tb["vp"],
+                                                 tb["pt"], tb["pl"], ob, False, wb), reps(50))
+        Pb = cb.prefix_len
+        pairs_b = sum((p_ + cb.D) * cb.D for p_ in Pb)
+        flops_b = 4.0 * cb.d * cb.Hq * pairs_b
+        bytes_b = (sum(Pb) * 2 * cb.Hkv * cb.d * 2.0 + cb.B * cb.D * (2 * cb.Hq + 2 * cb.Hkv) * cb.d * 2.0
+                   + cb.B * cb.pool.max_pages_per_seq * 4.0)
+        res["block_decode"] = with_kernel(
+            dict(roof(flops_b, bytes_b, ms_b), kernel_us=dict(time_calls.kernel_us),
+                 workload=f"batch 8, D=64 after prefixes uniform in {{512..4096}} (sum {sum(Pb)}), "
+                          "32/8 heads, d=128, page 16"), flops_b, bytes_b, "attention")
+        del tb, ob, wb, cb
 
     if want("extend"):
         # short causal extend: batch 64, 9 new tokens (2N-1, N = 5), prefixes at
@@ -752,8 +779,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    help="run only these secondary rows (comma list of prefill, qkv_post, extend, "
-                         "multicanvas, multicanvas_window) and print them; for profiler captures")
+                    help="run only these secondary rows (comma list of prefill, qkv_post, block_decode, "
+                         "extend, multicanvas, multicanvas_window) and print them; for profiler captures")
     ap.add_argument("--row-reps", type=int, default=0,
                     help="timed calls per secondary row (0: the row's default)")
     ap.add_argument("--row-batch", type=int, default=64,
