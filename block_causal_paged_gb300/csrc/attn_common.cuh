@@ -299,12 +299,26 @@ struct Planner {
   // --------------------------------------------------------------------------
   // Next work item from the shared counter (zero at launch: the last CTA of
   // the previous launch reset it, as does the plan kernel).
+  // Work units (CTAs, or CTA pairs) take their first item by their own
+  // index, without the counter's latency, and the rest from the counter,
+  // offset by the number of units: every item is handed out exactly once.
+  bool grabbed = false;
+  __device__ int units() const {
+    return kPair ? (int)(gridDim.x / 2) : (int)gridDim.x;
+  }
+  __device__ int next_index() {
+    if (!grabbed) {
+      grabbed = true;
+      return kPair ? (int)(blockIdx.x / 2) : (int)blockIdx.x;
+    }
+    return units() + atomicAdd(&p.hdr->work_next, 1);
+  }
   __device__ int grab() {
     if constexpr (kPair) {
       return grab_pair();
     } else {
       int idx = 0;
-      if (lane == 0) idx = atomicAdd(&p.hdr->work_next, 1);
+      if (lane == 0) idx = next_index();
       return __shfl_sync(0xffffffffu, idx, 0);
     }
   }
@@ -317,8 +331,9 @@ struct Planner {
   }
 
   // A CTA pair works on the same items: the first CTA takes the next index
-  // from the counter and posts it into a four-entry mailbox in the second
-  // CTA's shared memory; the second CTA reads its mailbox and frees the entry.
+  // (its own pair index first, then from the counter) and posts it into a
+  // four-entry mailbox in the second CTA's shared memory; the second CTA
+  // reads its mailbox and frees the entry.
   uint32_t n_grab = 0;
   __device__ int grab_pair() {
     const uint32_t k = n_grab++;
@@ -329,7 +344,7 @@ struct Planner {
         ok = false;
       } else {
         if (lane == 0) {
-          idx = atomicAdd(&p.hdr->work_next, 1);
+          idx = next_index();
           st_shared_cluster_u32(mapa_shared(smem_u32(&c.mail[slot]), 1), (uint32_t)idx);
           mbar_arrive_remote(mapa_shared(smem_u32(&c.bar.mail_full[slot]), 1));
         }
@@ -417,27 +432,29 @@ struct Planner {
     const int sb0 = (int)warp_excl_scan_ll(sz0 + sz1, lane);
     const int sb[2] = {sb0, sb0 + sz0};
     const long long n_slots = warp_sum_ll(sz0 + sz1);
-    if (blockIdx.x == 0) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int b = 2 * lane + k;
-        if (b >= B) continue;
-        p.split_base[b] = sb[k];
-        if (nch[k] <= 1) continue;
-        for (int gr = 0; gr < per_seq; ++gr) {
-          const int first = sb[k] + gr * nch[k];
-          for (int cc = 0; cc < nch[k]; ++cc)
-            if (first + cc < p.split_cap)
-              p.slot_info[first + cc] =
-                  make_int4(b, ((gr / p.n_rb) << 16) | (gr % p.n_rb), first, nch[k]);
+    // The split slots' table, read only by the epilogue kernel: sequence b's
+    // entries are written by CTA b (modulo the grid), its lanes in parallel,
+    // so that no CTA's first item waits for the whole table
+    for (int bb = blockIdx.x; bb < B; bb += gridDim.x) {
+      const int o = bb >> 1, kk = bb & 1;  // the lane and register holding sequence bb
+      const int nchb = __shfl_sync(0xffffffffu, kk ? nch[1] : nch[0], o);
+      const int sbb = __shfl_sync(0xffffffffu, kk ? sb[1] : sb[0], o);
+      if (lane == 0) p.split_base[bb] = sbb;
+      if (nchb > 1) {
+        for (int e = lane; e < per_seq * nchb; e += 32) {
+          const int gr = e / nchb, cc = e % nchb;
+          const int first = sbb + gr * nchb;
+          if (first + cc < p.split_cap)
+            p.slot_info[first + cc] =
+                make_int4(bb, ((gr / p.n_rb) << 16) | (gr % p.n_rb), first, nchb);
         }
       }
-      if (lane == 0) {
-        p.hdr->chunk_tiles = CH;
-        p.hdr->n_items = n_items;
-        p.hdr->n_split_slots = (int)(n_slots < p.split_cap ? n_slots : p.split_cap);
-        if (n_slots > p.split_cap || n_all > p.items_cap) record_error(p, kErrWorkspace);
-      }
+    }
+    if (blockIdx.x == 0 && lane == 0) {
+      p.hdr->chunk_tiles = CH;
+      p.hdr->n_items = n_items;
+      p.hdr->n_split_slots = (int)(n_slots < p.split_cap ? n_slots : p.split_cap);
+      if (n_slots > p.split_cap || n_all > p.items_cap) record_error(p, kErrWorkspace);
     }
     while (ok) {
       const int idx = grab();
