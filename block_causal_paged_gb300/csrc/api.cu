@@ -512,6 +512,7 @@ int decode_impl(const bca_dims* d, const void* q, const void* k_blk, const void*
   p.v_dense = (const uint16_t*)v_blk;
   p.dense_tokens = (int)q_tokens;
   p.out = (uint16_t*)out;
+  p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.hdr = (WsHeader*)ws;
   p.split_base = (int32_t*)((char*)ws + lay.split_base_off);
   p.items = (int4*)((char*)ws + lay.items_off);
@@ -617,6 +618,7 @@ int bca_prefill(const bca_dims* d, const void* q, const void* k, const void* v,
   p.v_dense = (const uint16_t*)v;
   p.dense_tokens = total_tokens;
   p.out = (uint16_t*)out;
+  p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.hdr = (WsHeader*)ws;
 
   AttnMaps maps;
@@ -722,6 +724,7 @@ int multicanvas_impl(const bca_dims* d, const void* q_live, const void* k_live,
   p.v_dense = (const uint16_t*)v_live;
   p.dense_tokens = (int)q_tokens;
   p.out = (uint16_t*)out;
+  p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.hdr = (WsHeader*)ws;
   p.tile_kv = (int2*)((char*)ws + kWsHeaderBytes);
   p.n_at_max = ceil_div_i((long long)d->max_pages_per_seq * d->page_size, kTileKeys);

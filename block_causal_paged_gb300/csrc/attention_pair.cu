@@ -574,21 +574,28 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
 #pragma unroll 1
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t o1[32], o2[32];
-        tmem_ld32_sync(t_lo + cb + c0, o1);
-        tmem_ld32_sync(t_hi + cb + c0, o2);
+        tmem_ld32x2_sync(t_lo + cb + c0, t_hi + cb + c0, o1, o2);
         if (valid) {
+          // the row's 32 columns as bf16: two 32-byte stores (16-byte ones
+          // when the output is only 16-byte aligned)
+          uint32_t w[16];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float f[8];
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(
+                __uint_as_float(o1[2 * i]) * s_lo + __uint_as_float(o2[2 * i]) * s_hi,
+                __uint_as_float(o1[2 * i + 1]) * s_lo + __uint_as_float(o2[2 * i + 1]) * s_hi);
+          if (p.out_align32) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              f[i] = __uint_as_float(o1[8 * k + i]) * s_lo + __uint_as_float(o2[8 * k + i]) * s_hi;
-            uint4 v;
-            v.x = pack_bf16x2(f[0], f[1]);
-            v.y = pack_bf16x2(f[2], f[3]);
-            v.z = pack_bf16x2(f[4], f[5]);
-            v.w = pack_bf16x2(f[6], f[7]);
-            *reinterpret_cast<uint4*>(dst + c0 + 8 * k) = v;
+            for (int k = 0; k < 2; ++k) {
+              const uint32_t v8[8] = {w[8 * k], w[8 * k + 1], w[8 * k + 2], w[8 * k + 3],
+                                      w[8 * k + 4], w[8 * k + 5], w[8 * k + 6], w[8 * k + 7]};
+              st_global_v8(dst + c0 + 16 * k, v8);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<uint4*>(dst + c0 + 8 * k) =
+                  make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
           }
         }
       }
@@ -598,8 +605,7 @@ __device__ __forceinline__ void run_softmax(const PCtx& c, const AttnParams& p, 
 #pragma unroll 1
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t o1[32], o2[32];
-        tmem_ld32_sync(t_lo + cb + c0, o1);
-        tmem_ld32_sync(t_hi + cb + c0, o2);
+        tmem_ld32x2_sync(t_lo + cb + c0, t_hi + cb + c0, o1, o2);
         if (valid) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {

@@ -84,6 +84,7 @@ struct AttnParams {
   int pool_rows;             // num_pages * Hkv * S
   int dense_tokens;          // token rows of the dense K/V view
   uint16_t* out;             // bf16 [q_tokens, Hq, d]
+  int out_align32;           // out is 32-byte aligned: the pair kernel stores 32 bytes at a time
   WsHeader* hdr;
   int32_t* split_base;
   int4* items;               // decode: item list written by the plan kernel

@@ -179,3 +179,21 @@ def test_pair_decode_ragged_chunks(cuda_lib, P, D):
     gd = rd.run().clone()
     assert rd.status() == 0
     assert_close(gd, _decode_ref(cd), what=f"pair decode P={Pd} D={D}")
+
+
+def test_pair_output_only_16_byte_aligned(cuda_lib):
+    """The pair kernel stores each row's output 32 bytes at a time when the
+    output is 32-byte aligned, 16 bytes at a time otherwise: an output buffer
+    offset by 16 bytes gets the same bits as an aligned one."""
+    case = workloads.make_decode_case([1024, 64 * 9, 4096], D=64, Hq=32, Hkv=8, d=128, seed=21)
+    r = DecodeRun(case)
+    ref = r.run().clone()
+    assert r.status() == 0
+    assert r.out.data_ptr() % 32 == 0
+    flat = torch.empty(r.out.numel() + 8, dtype=r.out.dtype, device=r.out.device)
+    r.out = flat[8:].view(r.out.shape)
+    assert r.out.data_ptr() % 32 == 16
+    got = r.run()
+    assert r.status() == 0
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert_close(got, _decode_ref(case), what="pair decode, 16-byte aligned output")
