@@ -55,6 +55,38 @@ def test_multicanvas_b16(cuda_lib, seed):
     assert np.array_equal(r.arena_len.cpu().numpy(), alen)
 
 
+def _degenerate_case():
+    """Four sequences: one with no live rows (nothing to attend to or
+    promote), one whose arena is empty (its live rows see only each other),
+    two ordinary ones."""
+    c = workloads.make_multicanvas_case(4, 128, 3, 64, Hq=32, Hkv=8, d=128, seed=9)
+    c.live_count[1] = 0
+    c.commit_count[1] = 0
+    c.arena_len[2] = 0
+    c.arena_k[2], c.arena_v[2], c.arena_pos[2] = c.arena_k[2][:0], c.arena_v[2][:0], c.arena_pos[2][:0]
+    return c
+
+
+def test_no_live_rows_and_empty_arena(cuda_lib):
+    c = _degenerate_case()
+    r = MulticanvasRun(c)
+    out = r.run()
+    assert r.status() == 0
+    m = _live_mask(c)
+    assert_close(out.cpu()[torch.from_numpy(m)], _ref(c)[m], what="no live rows / empty arena")
+    k, v, kv_pos, alen = _expected_promotion(c)
+    assert np.array_equal(r.k_pool.cpu().view(torch.int16).numpy(), k)
+    assert np.array_equal(r.v_pool.cpu().view(torch.int16).numpy(), v)
+    assert np.array_equal(r.kv_pos.cpu().numpy(), kv_pos)
+    assert np.array_equal(r.arena_len.cpu().numpy(), alen)
+    # the same under a narrow sliding window (band kernel)
+    c = _degenerate_case()
+    r = MulticanvasRun(c, promote=False)
+    out = r.run(window=64)
+    assert r.status() == 0
+    assert_close(out.cpu()[torch.from_numpy(m)], _ref(c, 64)[m], what="window 64, degenerate")
+
+
 def test_multicanvas_small_shapes(cuda_lib):
     c = workloads.make_multicanvas_case(3, 40, 4, 24, Hq=6, Hkv=2, d=64, seed=5)
     r = MulticanvasRun(c)

@@ -19,6 +19,7 @@ def _ref(case, q_rows=None):
     ([257, 128, 5], 16, 8, 2, 64),           # D = 16, head_dim 64, a 5-token prompt
     ([640, 130], 1, 4, 4, 128),              # block size 1 = causal attention, G = 1
     ([384], 384, 6, 2, 128),                 # one block = bidirectional, G = 3
+    ([0, 200, 0, 64], 64, 8, 2, 128),        # zero-length sequences among others
 ])
 def test_prefill_small(cuda_lib, lens, D, Hq, Hkv, d):
     case = workloads.make_prefill_case(lens, D=D, Hq=Hq, Hkv=Hkv, d=d, seed=21)
