@@ -94,7 +94,8 @@ struct AttnParams {
   float* part_o;
   int split_cap;
   // decode with commit: the block's K/V (k_dense / v_dense) is copied into
-  // these pools by the attention kernel itself (null: no commit)
+  // these pools by the decode epilogue kernel, after the attention kernel
+  // (null: no commit)
   uint16_t* commit_k;
   uint16_t* commit_v;
   // multicanvas: {smallest, largest} key position of arena tile a of sequence
