@@ -47,10 +47,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Commit of the blocks' K/V by CTAs first_cta .. gridDim.x-1: their warp w
-// copies token rows w, w + W, ...
+// copies token rows w, w + W, ... two at a time.  Both rows' K/V pieces are
+// loaded first (they do not depend on the destination), then both prefix
+// lengths, then both page-table entries, so that a pair of rows costs about
+// one memory round trip instead of three per row.
 template <int HD>
 __device__ __forceinline__ void commit_rows(const AttnParams& p, int first_cta) {
   constexpr int kPerHead = HD / 8;  // 16-byte pieces per head row
+  constexpr int kLane = 4;          // pieces per lane and row held in registers
   const int lane = threadIdx.x & 31;
   const int per_row = p.Hkv * kPerHead;
   const long long rows = (long long)p.B * p.Dblk;
@@ -60,32 +64,73 @@ __device__ __forceinline__ void commit_rows(const AttnParams& p, int first_cta) 
   const uint4* vs = reinterpret_cast<const uint4*>(p.v_dense);
   uint4* kd = reinterpret_cast<uint4*>(p.commit_k);
   uint4* vd = reinterpret_cast<uint4*>(p.commit_v);
-  for (long long row = warp; row < rows; row += n_warps) {
-    const int b = (int)(row / p.Dblk), t = (int)(row % p.Dblk);
-    const int P = __ldg(p.lens + b);
-    if (P < 0 || (!p.causal && P % p.Dblk != 0) ||
-        (long long)P + p.Dblk > (long long)p.max_pages * p.S)
-      continue;  // a bad prefix length is reported by the plan kernel
-    const int pos = P + t;
-    const int page = __ldg(p.page_table + (size_t)b * p.max_pages + pos / p.S);
-    if (page < 0 || page >= p.num_pages) {
-      if (lane == 0) atomicCAS(&p.hdr->status, 0, -16);  // page id outside the pool
-      continue;
+  // destination piece of piece i (head i / kPerHead) of a row at (page, slot)
+  auto dst_of = [&](int page, int slot, int i) {
+    return (((size_t)page * p.Hkv + i / kPerHead) * p.S + slot) * kPerHead + i % kPerHead;
+  };
+  for (long long row0 = warp; row0 < rows; row0 += 2 * n_warps) {
+    const long long rr[2] = {row0, row0 + n_warps};
+    uint4 kv[2][kLane], vv[2][kLane];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int u = 0; u < kLane; ++u) {
+        const int i = 32 * u + lane;
+        if (rr[j] < rows && i < per_row) {
+          kv[j][u] = __ldg(ks + rr[j] * per_row + i);
+          vv[j][u] = __ldg(vs + rr[j] * per_row + i);
+        }
+      }
+    int pos[2], page[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      pos[j] = -1;
+      if (rr[j] < rows) {
+        const int b = (int)(rr[j] / p.Dblk), t = (int)(rr[j] % p.Dblk);
+        const int P = __ldg(p.lens + b);
+        // a bad prefix length is reported by the plan kernel
+        if (P >= 0 && (p.causal || P % p.Dblk == 0) &&
+            (long long)P + p.Dblk <= (long long)p.max_pages * p.S)
+          pos[j] = P + t;
+      }
     }
-    const int slot = pos % p.S;
-    for (int i = lane; i < per_row; i += 32) {
-      const int h = i / kPerHead, cc = i % kPerHead;
-      const size_t dst = (((size_t)page * p.Hkv + h) * p.S + slot) * kPerHead + cc;
-      const uint4 kv = __ldg(ks + row * per_row + i);
-      const uint4 vv = __ldg(vs + row * per_row + i);
-      kd[dst] = kv;
-      vd[dst] = vv;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      page[j] = -1;
+      if (pos[j] >= 0) {
+        const int b = (int)(rr[j] / p.Dblk);
+        page[j] = __ldg(p.page_table + (size_t)b * p.max_pages + pos[j] / p.S);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (pos[j] < 0) continue;
+      if (page[j] < 0 || page[j] >= p.num_pages) {
+        if (lane == 0) atomicCAS(&p.hdr->status, 0, -16);  // page id outside the pool
+        continue;
+      }
+      const int slot = pos[j] % p.S;
+#pragma unroll
+      for (int u = 0; u < kLane; ++u) {
+        const int i = 32 * u + lane;
+        if (i < per_row) {
+          const size_t dst = dst_of(page[j], slot, i);
+          kd[dst] = kv[j][u];
+          vd[dst] = vv[j][u];
+        }
+      }
+      // rows wider than the registers' share (more than 8 KV heads at d = 128)
+      for (int i = 32 * kLane + lane; i < per_row; i += 32) {
+        const size_t dst = dst_of(page[j], slot, i);
+        kd[dst] = __ldg(ks + rr[j] * per_row + i);
+        vd[dst] = __ldg(vs + rr[j] * per_row + i);
+      }
     }
   }
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(const __grid_constant__ AttnParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kQ = HD / kCols;
