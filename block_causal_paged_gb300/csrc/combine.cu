@@ -4,9 +4,10 @@
 // Commit: the blocks' rows P .. P+D-1 are bit-copied from the dense block K/V
 // into their pages ("Inference for Interpretable Text-Diffusion Models", "KV
 // Cache": a final pass commits the block; "Paged Attention": position p lives
-// in page page_table[b][p / S], slot p % S); one warp per token row, 16-byte
-// accesses.  It runs after the attention kernel, which reads only rows below
-// P, and before anything later in the stream reads the pages.
+// in page page_table[b][p / S], slot p % S); a warp copies two token rows at
+// a time with 16-byte accesses.  It runs after the attention kernel, which
+// reads only rows below P, and before anything later in the stream reads the
+// pages.
 //
 // A long prefix is split into chunks that different CTAs attend to (each
 // chunk is an online softmax over its keys), so every row
@@ -18,11 +19,12 @@
 // Work unit: one split group (its first slot in the slot table) x 32 head-dim
 // columns; 256 threads, one per row (two M-tiles of 128), so every load of a
 // partial is 512 contiguous bytes per warp.  The (max, sum) pairs and partial
-// outputs of up to four chunks are loaded together and merged online (running
-// maximum, rescaled accumulator), so a unit costs about two memory round
-// trips.  Two CTAs per SM; the combine CTAs read the slot table in
-// coalesced chunks and keep only the first slot of each group.  Launched with programmatic dependent launch: the grid may start
-// while the attention kernel drains and waits for it to finish.
+// outputs of kBatch chunks are loaded together and merged online (running
+// maximum, rescaled accumulator), so a unit costs about one memory round trip
+// per kBatch chunks.  Two CTAs per SM; the combine CTAs read the slot table
+// in coalesced chunks and keep only the first slot of each group.  Launched
+// with programmatic dependent launch: the grid may start while the attention
+// kernel drains, and waits for it to finish.
 #include <cstdint>
 
 #include "bca_internal.h"
