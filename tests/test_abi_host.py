@@ -50,8 +50,8 @@ def _d(bca, **kw):
 
 
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(num_q_heads=30), dict(page_size=8),
-                                 dict(page_size=24), dict(block_size=0), dict(num_pages=0),
-                                 dict(softmax_scale=-1.0)])
+                                 dict(page_size=24), dict(page_size=272), dict(block_size=0),
+                                 dict(num_pages=0), dict(softmax_scale=-1.0)])
 def test_invalid_dims_rejected_without_launch(bca, bad):
     d = _d(bca, **bad)
     assert bca.workspace_size(d, bca.OP_DECODE) == 0
@@ -59,6 +59,12 @@ def test_invalid_dims_rejected_without_launch(bca, bad):
     p = ctypes.addressof(buf)
     rc = bca.load().bca_decode(ctypes.byref(d), p, p, p, p, p, p, p, p, 0, p, 1 << 20, None)
     assert rc == bca.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("S", [16, 32, 64, 128, 256])
+def test_page_sizes_accepted(bca, S):
+    """Any multiple of 16 from 16 to 256 tokens per page."""
+    assert bca.workspace_size(_d(bca, page_size=S), bca.OP_DECODE) > 0
 
 
 def test_wrong_abi_version_rejected(bca):
