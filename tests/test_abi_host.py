@@ -151,6 +151,17 @@ def test_product_package_never_imports_the_oracle():
                 assert "oracle" not in text.lower(), f
 
 
+def test_kernels_never_trap():
+    """No device code traps or asserts: a failure detected on the device is a
+    status word the host reads (bca_read_device_status), never a fault."""
+    import re
+    csrc = os.path.join(ROOT, "block_causal_paged_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        code = re.sub(r"//[^\n]*", "", open(os.path.join(csrc, f)).read())
+        assert "__trap" not in code and "brkpt" not in code, f
+        assert not re.search(r"(?<!static_)assert\s*\(", code), f
+
+
 def test_confidence_argument_errors(bca):
     """Host checks of bca_confidence that need no GPU."""
     import ctypes
